@@ -1,0 +1,200 @@
+"""CPU fp64 oracle for the In-Place TTT chunk-wise fast-weight (W_down) path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports, calls or links
+this module; only the tests, ``__graft_entry__.smoke()`` and the benchmark's
+CPU-baseline leg do.  It shares no code with the CUDA path: the only common
+module is the seeded input generator, which holds none of the method's
+arithmetic.
+
+It computes, in float64 on the same bf16/fp32-stored inputs the GPU sees,
+exactly what the method defines, step by step in the order the pages give it.
+numpy's matmul is the one library primitive used; nothing is blocked, fused or
+reordered beyond the definitions.
+
+Sources (titles of the pages; sections as printed on them):
+  [SUM]  "In-Place Test-Time Training", paperlayer.ai summary of arXiv
+         2604.06169v1 -- sections 3 (In-Place Adaptation, Chunk-Wise Updates,
+         LM-Aligned Objective), B (Context Parallel Algorithm), C.2, C.3.
+  [BLOG] iplexlaw.co.kr walkthrough of arXiv 2604.06169v1 -- sections 2, 3, 4, 6.
+
+Readings taken where the pages leave a step open (each is repeated in the
+design notes):
+  R1  The target convolution is a depthwise forward window that starts at the
+      next token: U[t] = sum_{j<k} conv[j] * X0[t+1+j], with every term whose
+      token lies at or past the end of t's chunk set to zero.  ("future-token
+      information", [SUM] 3 LM-Aligned Objective; "next token or a combination
+      of nearby future tokens", [BLOG] 4; no pull from other chunks, [BLOG] 6.)
+  R2  No bias in the convolution or in W_target (none is mentioned).
+  R3  The update is W <- W + eta * V^T Z with no 1/C factor ([BLOG] 2 and 4).
+  R4  Chunking restarts at every document start; a document's last chunk may
+      be shorter than C.  A call's trailing partial chunk is a short chunk.
+  R5  Update clipping ([SUM] C.2) is off on this path.
+
+Function-level parity status: every public function here is pinned by a
+"not gpu" test (brute force, closed forms, library routines, invariants).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "silu",
+    "swiglu_intermediate",
+    "chunk_target_source",
+    "chunk_target",
+    "chunk_spans",
+    "ttt_layer",
+    "ttt_layer_rows",
+    "rms_norm",
+    "ttt_stack",
+]
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+def silu(a: np.ndarray) -> np.ndarray:
+    """SiLU(a) = a * sigmoid(a) = a / (1 + exp(-a)).
+
+    SwiGLU activation ([SUM] C.3 "SwiGLU activations")."""
+    a = _f64(a)
+    return a / (1.0 + np.exp(-a))
+
+
+def swiglu_intermediate(x, w_gate, w_up) -> np.ndarray:
+    """Gated intermediate activation Z = SiLU(X W_gate^T) * (X W_up^T).
+
+    The two projections of the gated MLP are combined into Z; W_gate and W_up
+    stay frozen ([BLOG] 2; [SUM] 3 In-Place Adaptation).  x: n x d,
+    w_gate/w_up: f x d (nn.Linear layout) -> n x f."""
+    x = _f64(x)
+    return silu(x @ _f64(w_gate).T) * (x @ _f64(w_up).T)
+
+
+def chunk_target_source(x0_chunk, conv_w) -> np.ndarray:
+    """Depthwise causal-shifted Conv1D of one chunk's embeddings (reading R1).
+
+    U[t] = sum_{j=0}^{k-1} conv[j] (elementwise) X0[t+1+j], terms whose token
+    index t+1+j reaches the chunk's end are zero, so no information enters
+    from another chunk ([BLOG] 6; "causal padding", [SUM] B).
+    x0_chunk: n x d, conv_w: k x d -> n x d."""
+    x0 = _f64(x0_chunk)
+    cw = _f64(conv_w)
+    n, d = x0.shape
+    u = np.zeros((n, d), dtype=np.float64)
+    for j in range(cw.shape[0]):
+        m = n - (1 + j)  # tokens t with t+1+j < n
+        if m > 0:
+            u[:m] += cw[j][None, :] * x0[1 + j:1 + j + m]
+    return u
+
+
+def chunk_target(x0_chunk, conv_w, w_target) -> np.ndarray:
+    """LM-aligned target V = Conv1D(X0) W_target ([SUM] 3 LM-Aligned Objective;
+    [BLOG] 4).  w_target: d x d, given as in x out."""
+    return chunk_target_source(x0_chunk, conv_w) @ _f64(w_target)
+
+
+def chunk_spans(n_tokens: int, chunk: int, doc_starts=(0,)):
+    """Chunk boundaries of one call: list of (start, end, resets_w).
+
+    Non-overlapping chunks of ``chunk`` tokens processed in order ([SUM] 3
+    Chunk-Wise Updates); chunking restarts at each document start, where the
+    fast weight is reset ([SUM] B; reading R4).  The call itself starts a fresh
+    chunk at token 0 whether or not 0 is a document start."""
+    if chunk < 1:
+        raise ValueError("chunk must be >= 1")
+    starts = sorted(set(int(s) for s in (doc_starts or ())))
+    if any(s < 0 or s >= max(n_tokens, 1) for s in starts) and n_tokens > 0:
+        raise ValueError("document starts must lie in [0, n_tokens)")
+    cuts = [0] + [s for s in starts if s > 0] + [n_tokens]
+    spans = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        doc_reset = a in starts
+        t = a
+        while t < b:
+            e = min(t + chunk, b)
+            spans.append((t, e, doc_reset and t == a))
+            t = e
+    return spans
+
+
+def ttt_layer(x, x0, w_gate, w_up, w_down0, conv_w, w_target, eta, chunk,
+              doc_starts=(0,), w_init=None):
+    """One TTT-MLP layer over one call's tokens, the sequential recursion.
+
+    For every chunk c in order ([BLOG] 3 "apply then update"):
+      Z_c = SiLU(X_c W_gate^T) * (X_c W_up^T)
+      O_c = Z_c W_c^T                      (the state before this chunk's update)
+      V_c = Conv1D(X0_c) W_target          (chunk-local target)
+      W_{c+1} = W_c + eta V_c^T Z_c        ([BLOG] 2, 4)
+    W starts at ``w_init`` (default W_0 = w_down0) and is reset to W_0 at each
+    document start ([SUM] B).  Returns (O n x d, final W d x f), float64."""
+    x = _f64(x)
+    x0 = _f64(x0)
+    w0 = _f64(w_down0)
+    n = x.shape[0]
+    W = w0.copy() if w_init is None else _f64(w_init).copy()
+    out = np.zeros((n, w0.shape[0]), dtype=np.float64)
+    for s, e, reset in chunk_spans(n, chunk, doc_starts):
+        if reset:
+            W = w0.copy()
+        z = swiglu_intermediate(x[s:e], w_gate, w_up)
+        out[s:e] = z @ W.T
+        v = chunk_target(x0[s:e], conv_w, w_target)
+        W = W + float(eta) * (v.T @ z)
+    return out, W
+
+
+def ttt_layer_rows(x, x0, w_gate, w_up, w_down0, conv_w, w_target, eta, chunk,
+                   rows, doc_starts=(0,), w_init=None):
+    """The same recursion restricted to a subset of W's rows.
+
+    Row i of W, and column i of O, depend on all of Z but only on column i of
+    V (W[i] += eta * sum_t V[t,i] Z[t]; O[t,i] = Z[t] . W[i]).  So the sampled
+    rows are exact without computing the others.  Returns (O[:, rows],
+    W[rows])."""
+    rows = np.asarray(rows, dtype=np.int64)
+    x = _f64(x)
+    x0 = _f64(x0)
+    w0r = _f64(w_down0)[rows]
+    wt = _f64(w_target)[:, rows]
+    n = x.shape[0]
+    W = w0r.copy() if w_init is None else _f64(w_init)[rows].copy()
+    out = np.zeros((n, rows.size), dtype=np.float64)
+    for s, e, reset in chunk_spans(n, chunk, doc_starts):
+        if reset:
+            W = w0r.copy()
+        z = swiglu_intermediate(x[s:e], w_gate, w_up)
+        out[s:e] = z @ W.T
+        v = chunk_target_source(x0[s:e], conv_w) @ wt
+        W = W + float(eta) * (v.T @ z)
+    return out, W
+
+
+def rms_norm(h, eps=1e-6) -> np.ndarray:
+    """RMSNorm with unit gain: h / sqrt(mean(h^2) + eps), per row."""
+    h = _f64(h)
+    return h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + eps)
+
+
+def ttt_stack(h0, layers, eta, chunk, doc_starts=(0,), eps=1e-6, n_layers=None,
+              x0=None):
+    """Stack of pre-norm residual SwiGLU+TTT MLP blocks (no attention).
+
+    h_{l+1} = h_l + TTT_MLP_l(RMSNorm(h_l)) with X0 = h_0 for every layer
+    (X0 is the embedding sequence fed to the stack, [BLOG] 4).  ``x0`` is that
+    embedding sequence as stored for the layers (default: h0 itself).  Each
+    layer's recursion runs over all tokens before the next layer starts; that
+    is the same computation because nothing mixes tokens across layers except
+    the per-layer chunk recursion.  Returns (h_L, list of final W per layer)."""
+    h = _f64(h0).copy()
+    x0 = _f64(h0 if x0 is None else x0)
+    finals = []
+    for li, w in enumerate(layers[: n_layers or len(layers)]):
+        o, wf = ttt_layer(rms_norm(h, eps), x0, w["w_gate"], w["w_up"], w["w_down0"],
+                          w["conv_w"], w["w_target"], eta, chunk, doc_starts)
+        h = h + o
+        finals.append(wf)
+    return h, finals
