@@ -1,0 +1,241 @@
+// Plain CUDA-core kernels: the fp32 (FFMA) layer path, the chunk-local
+// Conv1D target source, state copies and conversions, and the residual-stack
+// glue.  The fp32 path computes every contraction in fp32 with no TF32.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace ttt {
+
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+constexpr int kMaxSpans = 256;
+
+// Token spans whose chunking is regular: span i covers [start[i], start[i] +
+// len[i]) and its chunks are [start + c*chunk, ...) clipped to the span end.
+struct SpanList {
+  int n;
+  int chunk;
+  int start[kMaxSpans];
+  int len[kMaxSpans];
+};
+
+// U[t] = sum_{j<k} conv[j] (.) X0[t+1+j] with every term at or past the end of
+// t's chunk dropped (chunk-local, causal-shifted depthwise Conv1D).  One
+// thread per (token, 8 channels).  Tokens outside every span are untouched.
+template <typename TIn, typename TOut>
+__global__ void conv_target_kernel(const TIn* __restrict__ x0, const TIn* __restrict__ conv_w,
+                                   TOut* __restrict__ u, int d, int k, const SpanList spans) {
+  const int groups_per_row = d / 8;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int first = spans.start[0];
+  const long long total =
+      (long long)(spans.start[spans.n - 1] + spans.len[spans.n - 1] - first) * groups_per_row;
+  if (idx >= total) return;
+  const int t = first + (int)(idx / groups_per_row);
+  const int c0 = (int)(idx % groups_per_row) * 8;
+  int lo = 0, hi = spans.n - 1;
+  while (lo < hi) {  // last span starting at or before t
+    const int mid = (lo + hi + 1) / 2;
+    if (spans.start[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int s0 = spans.start[lo];
+  const int cend = min(s0 + ((t - s0) / spans.chunk + 1) * spans.chunk, s0 + spans.len[lo]);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const int src = t + 1 + j;
+    if (src >= cend) break;
+    const TIn* xr = x0 + (size_t)src * d + c0;
+    const TIn* wr = conv_w + (size_t)j * d + c0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = fmaf(to_f(wr[e]), to_f(xr[e]), acc[e]);
+  }
+  TOut* ur = u + (size_t)t * d + c0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) ur[e] = from_f<TOut>(acc[e]);
+}
+
+// C(m,n) = alpha * sum_k A(m,k) B(k,n) + beta * C(m,n), fp32 accumulation.
+// A(m,k) = A[m*sam + k*sak], B(k,n) = B[k*sbk + n*sbn], C(m,n) = C[m*ldc + n].
+// 64x64 tiles, 256 threads, 4x4 outputs per thread, K staged 16 at a time.
+template <typename TA, typename TB, typename TC>
+__global__ void __launch_bounds__(256) simt_gemm_kernel(int M, int N, int K, const TA* __restrict__ A,
+                                                        long long sam, long long sak,
+                                                        const TB* __restrict__ B, long long sbk,
+                                                        long long sbn, TC* C, long long ldc,
+                                                        float alpha, float beta) {
+  __shared__ float As[16][64 + 1];
+  __shared__ float Bs[16][64 + 1];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int i = threadIdx.x; i < 16 * 64; i += 256) {
+      const int kk = i / 64, mm = i % 64;
+      const int m = m0 + mm, k = k0 + kk;
+      As[kk][mm] = (m < M && k < K) ? to_f(A[(long long)m * sam + (long long)k * sak]) : 0.0f;
+      const int n = n0 + mm;
+      Bs[kk][mm] = (n < N && k < K) ? to_f(B[(long long)k * sbk + (long long)n * sbn]) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty + 16 * i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx + 16 * j;
+      if (n >= N) continue;
+      TC* p = C + (long long)m * ldc + n;
+      float v = alpha * acc[i][j];
+      if (beta != 0.0f) v += beta * to_f(*p);
+      *p = from_f<TC>(v);
+    }
+  }
+}
+
+// Z(m,n) = SiLU(sum_k X(m,k) Wg(n,k)) * sum_k X(m,k) Wu(n,k); X: M x K, Wg/Wu: N x K.
+template <typename T>
+__global__ void __launch_bounds__(256) simt_swiglu_kernel(int M, int N, int K, const T* __restrict__ X,
+                                                          const T* __restrict__ Wg,
+                                                          const T* __restrict__ Wu,
+                                                          float* __restrict__ Z) {
+  __shared__ float Xs[16][64 + 1];
+  __shared__ float Gs[16][64 + 1];
+  __shared__ float Us[16][64 + 1];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  float ag[4][4] = {}, au[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int i = threadIdx.x; i < 16 * 64; i += 256) {
+      const int kk = i % 16, rr = i / 16;
+      const int k = k0 + kk;
+      const int m = m0 + rr, n = n0 + rr;
+      Xs[kk][rr] = (m < M && k < K) ? to_f(X[(long long)m * K + k]) : 0.0f;
+      Gs[kk][rr] = (n < N && k < K) ? to_f(Wg[(long long)n * K + k]) : 0.0f;
+      Us[kk][rr] = (n < N && k < K) ? to_f(Wu[(long long)n * K + k]) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], g[4], u[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = Xs[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        g[j] = Gs[kk][tx + 16 * j];
+        u[j] = Us[kk][tx + 16 * j];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          ag[i][j] = fmaf(a[i], g[j], ag[i][j]);
+          au[i][j] = fmaf(a[i], u[j], au[i][j]);
+        }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty + 16 * i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx + 16 * j;
+      if (n >= N) continue;
+      const float g = ag[i][j];
+      Z[(long long)m * N + n] = (g / (1.0f + expf(-g))) * au[i][j];
+    }
+  }
+}
+
+// dst[i] = float(src[i])  (fast-weight reset W <- W_0)
+template <typename T>
+__global__ void to_f32_kernel(const T* __restrict__ src, float* __restrict__ dst, long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] = to_f(src[i]);
+}
+
+// dst[i] = bf16(src[i])  (bf16 operand copy of the fp32 fast weight)
+__global__ void to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+                               long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] = __float2bfloat16_rn(src[i]);
+}
+
+// out[c, r] = in[r, c] for an R x Cc matrix (32x32 tiles through shared memory).
+template <typename T>
+__global__ void transpose_kernel(const T* __restrict__ in, T* __restrict__ out, int R, int Cc) {
+  __shared__ T tile[32][33];
+  const int c = blockIdx.x * 32 + threadIdx.x;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int r = blockIdx.y * 32 + i;
+    if (r < R && c < Cc) tile[i][threadIdx.x] = in[(long long)r * Cc + c];
+  }
+  __syncthreads();
+  const int r2 = blockIdx.y * 32 + threadIdx.x;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int c2 = blockIdx.x * 32 + i;
+    if (c2 < Cc && r2 < R) out[(long long)c2 * R + r2] = tile[threadIdx.x][i];
+  }
+}
+
+// x[t] = h[t] / sqrt(mean(h[t]^2) + eps); one block per row.
+template <typename TOut>
+__global__ void rmsnorm_kernel(const float* __restrict__ h, TOut* __restrict__ x, int d,
+                               float eps) {
+  const float* hr = h + (long long)blockIdx.x * d;
+  float ss = 0.0f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(hr[i], hr[i], ss);
+  __shared__ float red[32];
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = (threadIdx.x < blockDim.x / 32) ? red[threadIdx.x] : 0.0f;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float inv = rsqrtf(red[0] / (float)d + eps);
+  TOut* xr = x + (long long)blockIdx.x * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) xr[i] = from_f<TOut>(hr[i] * inv);
+}
+
+template <typename T>
+__global__ void residual_add_kernel(float* __restrict__ h, const T* __restrict__ o, long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    h[i] += to_f(o[i]);
+}
+
+}  // namespace ttt

@@ -1,0 +1,547 @@
+// Persistent, warp-specialised tcgen05 GEMM engine for the bf16 hot path.
+//
+// One CTA per SM, 192 threads:
+//   warp 0      TMA producer: takes tiles from a dynamic tile counter, streams
+//               the A/B operand blocks (64 K-elements each) into a 4-stage
+//               shared-memory ring with 128-byte swizzle.
+//   warp 1      owns the TMEM allocation (512 columns = two 128x256 fp32
+//               accumulators) and issues tcgen05.mma from one thread.
+//   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (one TMEM
+//               lane = one output row per thread), the mode's arithmetic, and
+//               global stores; the other accumulator is filled meanwhile.
+//
+// Modes (what the tiles are):
+//   kSwiGLU  Z = SiLU(X Wg^T) (.) (X Wu^T): the B tile stacks 128 rows of Wg
+//            and the same 128 rows of Wu, so one 128x256 accumulator holds the
+//            gate and up halves of a 128x128 block of Z.
+//   kVProj   V = eta * (U W_target) with U the chunk-local Conv1D output.
+//   kSGram   per group of chunks, S = Z_g Z_g^T with every entry whose column
+//            chunk is not strictly before its row chunk set to zero.
+//   kGroup   one group of G chunks: the apply tiles
+//              O_g = Z_g W_s^T + S_g V_g            (W_s = state at group start)
+//            and the update tiles
+//              W <- W_s + V_g^T Z_g,  Wb_next <- bf16(W)
+//            in one launch.  Applying W_s to every chunk of the group plus the
+//            intra-group correction S_g V_g equals applying each chunk's own
+//            pre-update state (the deltas are additive, appendix B of the
+//            "In-Place Test-Time Training" summary page).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda.h>
+#include <cstdint>
+
+#include "sm100_ptx.cuh"
+
+namespace ttt {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;          // 16 KB
+constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
+constexpr int kTmemCols = 2 * kBN;              // two fp32 accumulators
+constexpr int kSchedRing = 4;
+constexpr int kGemmThreads = 192;
+constexpr int kMaxGroups = 256;
+constexpr int kSwizzleGroupM = 16;
+
+enum GemmMode : int { kSwiGLU = 0, kVProj = 1, kSGram = 2, kGroup = 3 };
+
+// Tensor-map slots per mode.
+//   kSwiGLU: 0 X (box 64x128), 1 Wg (64x128), 2 Wu (64x128)
+//   kVProj:  0 U (64x128), 1 W_target^T (64x256)
+//   kSGram:  0 Z (64x128), 1 Z (64x256)
+//   kGroup:  0 Z (64x128), 1 W_s bf16 (64x256), 2 S (64x128),
+//            3 V MN-major (64x64), 4 V MN-major with the group's K extent,
+//            5 Z MN-major (64x64) with the group's K extent
+struct GemmArgs {
+  CUtensorMap map[6];
+  int n_rows;    // tokens of the call (rows of X/Z/U/V/O)
+  int d, f;
+  int chunk;
+  float alpha;   // eta for kVProj
+  int* counter;  // dynamic tile counter, zero at launch
+  int* err;      // workspace error word
+  void* out0;    // kSwiGLU: Z; kVProj: V; kSGram: S; kGroup: O
+  void* out1;    // kGroup: W (fp32, updated in place)
+  void* out2;    // kGroup: Wb_next (bf16)
+  const void* in0;  // kGroup: W_0 (bf16) when the group starts a document
+  // groups
+  int s_pad;         // row/column pitch of one S block (multiple of 256)
+  int n_groups;      // kSGram
+  int g_start[kMaxGroups];
+  int g_len[kMaxGroups];
+  int g0, glen, gslot, reset;  // kGroup
+};
+
+struct TileInfo {
+  int kind;  // 0 plain/apply, 1 update
+  int m0, n0;
+  int g;
+  int nkb1, nkb2;
+  bool valid;
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Exclusive end (multiple of 64) of the K range of the intra-group correction
+// for the 128-row tile m of a group of `len` tokens: the start of the chunk
+// that holds the tile's last row, rounded up to the K block.
+__device__ __forceinline__ int corr_kbound(int len, int m, int chunk) {
+  int last = min(m * kBM + kBM - 1, len - 1);
+  int cs = (last / chunk) * chunk;
+  return cdiv(cs, kBK) * kBK;
+}
+
+template <int MODE>
+__device__ __forceinline__ int num_tiles(const GemmArgs& a) {
+  if (MODE == kSwiGLU) return cdiv(a.n_rows, kBM) * cdiv(a.f, kBM);
+  if (MODE == kVProj) return cdiv(a.n_rows, kBM) * cdiv(a.d, kBN);
+  if (MODE == kSGram) return a.n_groups * cdiv(a.s_pad, kBM) * cdiv(a.s_pad, kBN);
+  return cdiv(a.glen, kBM) * cdiv(a.d, kBN) + cdiv(a.d, kBM) * cdiv(a.f, kBN);
+}
+
+template <int MODE>
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t) {
+  TileInfo ti{};
+  ti.valid = true;
+  ti.nkb2 = 0;
+  ti.kind = 0;
+  ti.g = 0;
+  if (MODE == kSwiGLU) {
+    const int mt = cdiv(a.n_rows, kBM), nt = cdiv(a.f, kBM);
+    const int gsz = kSwizzleGroupM * nt;
+    const int gid = t / gsz, first = gid * kSwizzleGroupM;
+    const int gm = min(kSwizzleGroupM, mt - first);
+    const int w = t % gsz;
+    ti.m0 = (first + w % gm) * kBM;
+    ti.n0 = (w / gm) * kBM;
+    ti.nkb1 = cdiv(a.d, kBK);
+  } else if (MODE == kVProj) {
+    const int nt = cdiv(a.d, kBN);
+    ti.m0 = (t / nt) * kBM;
+    ti.n0 = (t % nt) * kBN;
+    ti.nkb1 = cdiv(a.d, kBK);
+  } else if (MODE == kSGram) {
+    const int mt = cdiv(a.s_pad, kBM), nt = cdiv(a.s_pad, kBN);
+    const int g = t / (mt * nt), r = t % (mt * nt);
+    const int m = r / nt, n = r % nt;
+    const int len = a.g_len[g];
+    ti.g = g;
+    ti.m0 = m * kBM;
+    ti.n0 = n * kBN;
+    ti.valid = (ti.m0 < len) && (ti.n0 < corr_kbound(len, m, a.chunk));
+    ti.nkb1 = cdiv(a.f, kBK);
+  } else {
+    const int ntA = cdiv(a.d, kBN);
+    const int nA = cdiv(a.glen, kBM) * ntA;
+    if (t < nA) {
+      const int m = t / ntA;
+      ti.m0 = m * kBM;
+      ti.n0 = (t % ntA) * kBN;
+      ti.nkb1 = cdiv(a.f, kBK);
+      ti.nkb2 = corr_kbound(a.glen, m, a.chunk) / kBK;
+    } else {
+      const int u = t - nA, ntU = cdiv(a.f, kBN);
+      ti.kind = 1;
+      ti.m0 = (u / ntU) * kBM;
+      ti.n0 = (u % ntU) * kBN;
+      ti.nkb1 = cdiv(a.glen, kBK);
+    }
+  }
+  return ti;
+}
+
+// Issue the TMA loads of K block `kb` of tile `ti` into stage buffers sa / sb.
+template <int MODE>
+__device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& ti, int kb,
+                                            uint8_t* sa, uint8_t* sb, uint64_t* bar) {
+  if (MODE == kSwiGLU) {
+    tma_load_2d(sa, &a.map[0], bar, kb * kBK, ti.m0);
+    tma_load_2d(sb, &a.map[1], bar, kb * kBK, ti.n0);
+    tma_load_2d(sb + kBBytes / 2, &a.map[2], bar, kb * kBK, ti.n0);
+  } else if (MODE == kVProj) {
+    tma_load_2d(sa, &a.map[0], bar, kb * kBK, ti.m0);
+    tma_load_2d(sb, &a.map[1], bar, kb * kBK, ti.n0);
+  } else if (MODE == kSGram) {
+    const int gs = a.g_start[ti.g];
+    tma_load_2d(sa, &a.map[0], bar, kb * kBK, gs + ti.m0);
+    tma_load_2d(sb, &a.map[1], bar, kb * kBK, gs + ti.n0);
+  } else {
+    if (ti.kind == 0) {
+      if (kb < ti.nkb1) {
+        tma_load_2d(sa, &a.map[0], bar, kb * kBK, a.g0 + ti.m0);
+        tma_load_2d(sb, &a.map[1], bar, kb * kBK, ti.n0);
+      } else {
+        const int k2 = (kb - ti.nkb1) * kBK;
+        tma_load_2d(sa, &a.map[2], bar, k2, a.gslot * a.s_pad + ti.m0);
+#pragma unroll
+        for (int q = 0; q < kBN / 64; ++q)
+          tma_load_2d(sb + q * 8192, &a.map[3], bar, ti.n0 + q * 64, a.g0 + k2);
+      }
+    } else {
+      const int k = a.g0 + kb * kBK;
+#pragma unroll
+      for (int q = 0; q < kBM / 64; ++q)
+        tma_load_2d(sa + q * 8192, &a.map[4], bar, ti.m0 + q * 64, k);
+#pragma unroll
+      for (int q = 0; q < kBN / 64; ++q)
+        tma_load_2d(sb + q * 8192, &a.map[5], bar, ti.n0 + q * 64, k);
+    }
+  }
+}
+
+// Operand majors of K block kb: 0 = both K-major, 1 = B MN-major, 2 = both MN-major.
+template <int MODE>
+__device__ __forceinline__ int kblock_layout(const TileInfo& ti, int kb) {
+  if (MODE != kGroup) return 0;
+  if (ti.kind == 1) return 2;
+  return kb < ti.nkb1 ? 0 : 1;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+// Store 32 consecutive bf16 values (packed in 16 words) if the 8-groups are in range.
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t (&p)[16],
+                                              int cols_left) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (q * 8 < cols_left) {
+      uint4 v = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+      *reinterpret_cast<uint4*>(dst + q * 8) = v;
+    }
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo& ti,
+                                              uint32_t tacc, int row) {
+  uint32_t r[32];
+  if (MODE == kSwiGLU) {
+    const int grow = ti.m0 + row;
+    __nv_bfloat16* zrow = reinterpret_cast<__nv_bfloat16*>(a.out0) + (size_t)grow * a.f;
+#pragma unroll 1
+    for (int s = 0; s < kBM / 32; ++s) {
+      uint32_t u[32];
+      tmem_ld32(tacc + s * 32, r);
+      tmem_ld_wait(r);
+      tmem_ld32(tacc + kBM + s * 32, u);
+      tmem_ld_wait(u);
+      uint32_t p[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float z0 = silu_f(__uint_as_float(r[2 * j])) * __uint_as_float(u[2 * j]);
+        float z1 = silu_f(__uint_as_float(r[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+        p[j] = pack_bf16x2(z0, z1);
+      }
+      const int col = ti.n0 + s * 32;
+      if (grow < a.n_rows) store_bf16x32(zrow + col, p, a.f - col);
+    }
+  } else if (MODE == kVProj || MODE == kGroup) {
+    if (MODE == kGroup && ti.kind == 1) {
+      // fast-weight update: W <- base + acc; Wb_next <- bf16(W)
+      const int wr = ti.m0 + row;
+      float* wrow = reinterpret_cast<float*>(a.out1) + (size_t)wr * a.f;
+      __nv_bfloat16* brow = reinterpret_cast<__nv_bfloat16*>(a.out2) + (size_t)wr * a.f;
+      const __nv_bfloat16* w0row =
+          reinterpret_cast<const __nv_bfloat16*>(a.in0) + (size_t)wr * a.f;
+#pragma unroll 1
+      for (int s = 0; s < kBN / 32; ++s) {
+        const int col = ti.n0 + s * 32;
+        tmem_ld32(tacc + s * 32, r);
+        tmem_ld_wait(r);
+        if (wr >= a.d) continue;
+        float base[32];
+        if (a.reset) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (col + q * 8 < a.f) {
+              uint4 v = *reinterpret_cast<const uint4*>(w0row + col + q * 8);
+              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float2 ff = __bfloat1622float2(h[e]);
+                base[q * 8 + 2 * e] = ff.x;
+                base[q * 8 + 2 * e + 1] = ff.y;
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (col + q * 4 < a.f) {
+              float4 v = *reinterpret_cast<const float4*>(wrow + col + q * 4);
+              base[4 * q] = v.x;
+              base[4 * q + 1] = v.y;
+              base[4 * q + 2] = v.z;
+              base[4 * q + 3] = v.w;
+            }
+          }
+        }
+        float w[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) w[j] = base[j] + __uint_as_float(r[j]);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (col + q * 4 < a.f)
+            *reinterpret_cast<float4*>(wrow + col + q * 4) =
+                make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
+        uint32_t p[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) p[j] = pack_bf16x2(w[2 * j], w[2 * j + 1]);
+        store_bf16x32(brow + col, p, a.f - col);
+      }
+    } else {
+      // plain bf16 store of alpha * acc (kVProj) or acc (kGroup apply)
+      const float alpha = (MODE == kVProj) ? a.alpha : 1.0f;
+      const int grow = (MODE == kVProj) ? ti.m0 + row : a.g0 + ti.m0 + row;
+      const bool ok = (MODE == kVProj) ? (grow < a.n_rows) : (ti.m0 + row < a.glen);
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out0) + (size_t)grow * a.d;
+#pragma unroll 1
+      for (int s = 0; s < kBN / 32; ++s) {
+        tmem_ld32(tacc + s * 32, r);
+        tmem_ld_wait(r);
+        uint32_t p[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          p[j] = pack_bf16x2(alpha * __uint_as_float(r[2 * j]),
+                             alpha * __uint_as_float(r[2 * j + 1]));
+        const int col = ti.n0 + s * 32;
+        if (ok) store_bf16x32(orow + col, p, a.d - col);
+      }
+    }
+  } else {  // kSGram
+    const int len = a.g_len[ti.g];
+    const int i = ti.m0 + row;
+    const int ci = i / a.chunk;
+    __nv_bfloat16* srow =
+        reinterpret_cast<__nv_bfloat16*>(a.out0) + ((size_t)ti.g * a.s_pad + i) * a.s_pad;
+#pragma unroll 1
+    for (int s = 0; s < kBN / 32; ++s) {
+      tmem_ld32(tacc + s * 32, r);
+      tmem_ld_wait(r);
+      const int j0 = ti.n0 + s * 32;
+      uint32_t p[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int ja = j0 + 2 * j, jb = ja + 1;
+        const bool ka = (i < len) && (ja < len) && (ja / a.chunk < ci);
+        const bool kb = (i < len) && (jb < len) && (jb / a.chunk < ci);
+        p[j] = pack_bf16x2(ka ? __uint_as_float(r[2 * j]) : 0.0f,
+                           kb ? __uint_as_float(r[2 * j + 1]) : 0.0f);
+      }
+      if (i < a.s_pad) store_bf16x32(srow + j0, p, a.s_pad - j0);
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ GemmArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* stage_base = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = bars;                       // [kStages]
+  uint64_t* empty = full + kStages;            // [kStages]
+  uint64_t* acc_full = empty + kStages;        // [2]
+  uint64_t* acc_empty = acc_full + 2;          // [2]
+  uint64_t* sched_full = acc_empty + 2;        // [kSchedRing]
+  uint64_t* sched_empty = sched_full + kSchedRing;  // [kSchedRing]
+  uint64_t* drain = sched_empty + kSchedRing;  // [1]
+  int* sched_item = reinterpret_cast<int*>(drain + 1);  // [kSchedRing]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sched_item + kSchedRing);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int ntiles = num_tiles<MODE>(a);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    for (int s = 0; s < kSchedRing; ++s) {
+      mbar_init(&sched_full[s], 1);
+      mbar_init(&sched_empty[s], 5);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer + tile scheduler
+#pragma unroll 1
+      for (int q = 0; q < 6; ++q) tma_prefetch_desc(&a.map[q]);
+      int stage = 0;
+      uint32_t phase = 0;
+      int fills = 0;
+      bool ok = true;
+#pragma unroll 1
+      for (int it = 0; ok; ++it) {
+        const int slot = it % kSchedRing;
+        const uint32_t sp = (it / kSchedRing) & 1;
+        if (!mbar_wait(&sched_empty[slot], sp ^ 1, abort_flag, a.err, kErrWaitSched)) break;
+        const int t = atomicAdd(a.counter, 1);
+        sched_item[slot] = t;
+        mbar_arrive(&sched_full[slot]);
+        if (t >= ntiles) break;
+        const TileInfo ti = decode_tile<MODE>(a, t);
+        if (!ti.valid) continue;
+        const int nkb = ti.nkb1 + ti.nkb2;
+#pragma unroll 1
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.err, kErrWaitSmemEmpty)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = stage_base + stage * kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          load_kblock<MODE>(a, ti, kb, sa, sa + kABytes, &full[stage]);
+          ++fills;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (*abort_flag) {
+        // let every load still in flight land before the CTA's smem is released
+        for (int s = 0; s < kStages && s < fills; ++s) {
+          const uint32_t p = (s < stage) ? phase : (phase ^ 1);
+          volatile int never = 0;
+          mbar_wait(&full[s], p, &never, a.err, kErrWaitDrain);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc_it = 0;
+      bool ok = true;
+#pragma unroll 1
+      for (int it = 0; ok; ++it) {
+        const int slot = it % kSchedRing;
+        if (!mbar_wait(&sched_full[slot], (it / kSchedRing) & 1, abort_flag, a.err,
+                       kErrWaitSched))
+          break;
+        const int t = sched_item[slot];
+        mbar_arrive(&sched_empty[slot]);
+        if (t >= ntiles) break;
+        const TileInfo ti = decode_tile<MODE>(a, t);
+        if (!ti.valid) continue;
+        const int buf = acc_it & 1;
+        if (!mbar_wait(&acc_empty[buf], ((acc_it >> 1) & 1) ^ 1, abort_flag, a.err,
+                       kErrWaitAccEmpty))
+          break;
+        tc_fence_after();
+        const uint32_t tacc = tmem_base + buf * kBN;
+        const int nkb = ti.nkb1 + ti.nkb2;
+#pragma unroll 1
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, a.err, kErrWaitTmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(stage_base + stage * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+          const int lay = kblock_layout<MODE>(ti, kb);
+          const uint32_t idesc = idesc_bf16_f32(kBM, kBN, lay == 2, lay >= 1);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = (lay == 2) ? sdesc_sw128(sa + k * 2048, 8192, 1024)
+                                           : sdesc_sw128(sa + k * 32, 0, 1024);
+            const uint64_t bd = (lay >= 1) ? sdesc_sw128(sb + k * 2048, 8192, 1024)
+                                           : sdesc_sw128(sb + k * 32, 0, 1024);
+            tc_mma_bf16(tacc, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[buf]);
+        ++acc_it;
+      }
+      if (*abort_flag) {
+        tc_commit(drain);
+        volatile int never = 0;
+        mbar_wait(drain, 0, &never, a.err, kErrWaitDrain);
+      }
+    }
+  } else {
+    // ---------------- epilogue warps
+    const int sub = warp & 3;  // TMEM sub-partition this warp may access
+    const int row = sub * 32 + lane;
+    int acc_it = 0;
+#pragma unroll 1
+    for (int it = 0;; ++it) {
+      // lane 0 waits; the result is broadcast so the warp stays converged for
+      // the .sync.aligned TMEM loads
+      const int slot = it % kSchedRing;
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_wait(&sched_full[slot], (it / kSchedRing) & 1, abort_flag, a.err, kErrWaitSched);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const int t = sched_item[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sched_empty[slot]);
+      if (t >= ntiles) break;
+      const TileInfo ti = decode_tile<MODE>(a, t);
+      if (!ti.valid) continue;
+      const int buf = acc_it & 1;
+      if (lane == 0)
+        ok = mbar_wait(&acc_full[buf], (acc_it >> 1) & 1, abort_flag, a.err, kErrWaitAccFull);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + buf * kBN;
+      epilogue_tile<MODE>(a, ti, tacc, row);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      ++acc_it;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+
+}  // namespace ttt

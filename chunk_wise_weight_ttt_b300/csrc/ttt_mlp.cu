@@ -1,0 +1,791 @@
+// Host side of the C ABI declared in include/ttt_mlp.h: argument checks,
+// workspace carving, chunk/group planning, tensor-map encoding and kernel
+// launches for the two kernel families (tcgen05 bf16 path, fp32 SIMT path).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "ttt_mlp.h"
+#include "simt_kernels.cuh"
+#include "tc_gemm.cuh"
+
+using namespace ttt;
+
+struct ttt_mlp {
+  ttt_mlp_config cfg;
+  const void *wg, *wu, *w0, *conv, *wt;
+  uint8_t* ws;
+  size_t ws_bytes;
+  bool tc;
+  int G, L, s_pad, s_slots, num_sms;
+  float* W;                 // n_docs x d x f
+  __nv_bfloat16* Wb[2];     // bf16 operand copies of the current state
+  __nv_bfloat16* WtT;       // W_target transposed (out x in)
+  void *Z, *U, *V;          // per-call intermediates (n x f, n x d, n x d)
+  __nv_bfloat16* S;         // s_slots blocks of s_pad x s_pad
+  void *xs, *x0s, *os;      // host-staging copies of x, x0, o
+  int* ctrl;                // [0] error word, [64..] tile counters
+  int counter_next;
+  int wb_owner;             // slot whose state Wb[wb_cur] holds, -1 = none
+  int wb_cur;
+  CUtensorMap map_wg, map_wu, map_wtT, map_s, map_w0, map_wb[2];
+  std::string err;
+  // benchmark phase timing
+  bool profiling;
+  struct Rec {
+    int phase;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  int64_t prof_calls, prof_group_launches, prof_launches;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+constexpr int kCtrlInts = 4096;
+constexpr int kCounterBase = 64;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool fault_injected(const char* name) {
+  const char* f = std::getenv("TTT_FAULT");
+  return f && std::strcmp(f, name) == 0;
+}
+
+bool force_simt() {
+  const char* f = std::getenv("TTT_FORCE_SIMT");
+  return f && f[0] == '1';
+}
+
+struct Layout {
+  bool tc;
+  int G, L, s_pad, s_slots;
+  size_t ctrl, W, Wb0, Wb1, WtT, Z, U, V, S, xs, x0s, os, total;
+};
+
+bool config_ok(const ttt_mlp_config* c, std::string* why) {
+  auto bad = [&](const char* m) {
+    if (why) *why = m;
+    return false;
+  };
+  if (!c) return bad("config is NULL");
+  if (c->d < 8 || c->d % 8) return bad("d must be a positive multiple of 8");
+  if (c->f < 8 || c->f % 8) return bad("f must be a positive multiple of 8");
+  if (c->chunk < 1 || c->chunk > 1024) return bad("chunk must be in 1..1024");
+  if (c->conv_k < 1 || c->conv_k > 8) return bad("conv_k must be in 1..8");
+  if (c->n_docs < 1 || c->n_docs > 4096) return bad("n_docs must be in 1..4096");
+  if (c->act_dtype != TTT_F32 && c->act_dtype != TTT_BF16) return bad("act_dtype must be TTT_F32 or TTT_BF16");
+  if (c->max_tokens < 1 || c->max_tokens > (int64_t(1) << 24)) return bad("max_tokens must be in 1..2^24");
+  if (!std::isfinite(c->eta)) return bad("eta must be finite");
+  return true;
+}
+
+bool tc_shape_ok(const ttt_mlp_config& c) {
+  return c.act_dtype == TTT_BF16 && c.d % 64 == 0 && c.f % 64 == 0 && c.d >= 256 && c.f >= 256;
+}
+
+Layout make_layout(const ttt_mlp_config& c, bool tc) {
+  Layout l{};
+  l.tc = tc;
+  const size_t act = (c.act_dtype == TTT_BF16) ? 2 : 4;
+  const size_t inter = tc ? 2 : 4;
+  const size_t d = c.d, f = c.f, n = (size_t)c.max_tokens;
+  l.G = tc ? std::max(1, 1024 / c.chunk) : 1;
+  l.L = l.G * c.chunk;
+  l.s_pad = (int)align_up((size_t)l.L, 256);
+  l.s_slots = tc ? (int)std::min<int64_t>(kMaxGroups, (c.max_tokens + l.L - 1) / l.L + 4) : 0;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  l.ctrl = take(kCtrlInts * sizeof(int));
+  l.W = take((size_t)c.n_docs * d * f * 4);
+  l.Wb0 = tc ? take(d * f * 2) : 0;
+  l.Wb1 = tc ? take(d * f * 2) : 0;
+  l.WtT = tc ? take(d * d * 2) : 0;
+  l.Z = take(n * f * inter);
+  l.U = take(n * d * inter);
+  l.V = take(n * d * inter);
+  l.S = tc ? take((size_t)l.s_slots * l.s_pad * l.s_pad * 2) : 0;
+  l.xs = take(n * d * act);
+  l.x0s = take(n * d * act);
+  l.os = take(n * d * act);
+  l.total = o;
+  return l;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// bf16 matrix [outer x inner] row-major with row pitch `pitch` elements; box
+// (box_inner x box_outer) with 128-byte swizzle, zero fill outside.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
+              uint32_t box_inner, uint32_t box_outer, std::string* why) {
+  auto fn = encode_fn();
+  if (!fn) {
+    *why = "cuTensorMapEncodeTiled is unavailable";
+    return false;
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[160];
+    std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for a %llux%llu map",
+                  (int)r, (unsigned long long)outer, (unsigned long long)inner);
+    *why = buf;
+    return false;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- errors
+
+ttt_status fail(ttt_mlp* h, ttt_status s, const std::string& msg) {
+  if (h)
+    h->err = msg;
+  else
+    g_err = msg;
+  return s;
+}
+
+#define TTT_CK(h, expr)                                                                    \
+  do {                                                                                     \
+    cudaError_t e_ = (expr);                                                               \
+    if (e_ != cudaSuccess)                                                                 \
+      return fail((h), TTT_ECUDA, std::string(#expr) + ": " + cudaGetErrorString(e_));     \
+  } while (0)
+
+#define TTT_CK_LAUNCH(h) TTT_CK(h, cudaGetLastError())
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int grid_for(long long n, int block) {
+  long long g = (n + block - 1) / block;
+  return (int)std::max<long long>(1, std::min<long long>(g, 1 << 20));
+}
+
+// ---------------------------------------------------------------- planning
+
+struct Span {
+  int start, len;
+  bool reset;
+};
+
+// Chunks of one call (a document start restarts the chunking; the call starts
+// a fresh chunk at token 0), then groups of up to G consecutive chunks of one
+// document.  Only a group's last chunk can be shorter than C.
+std::vector<Span> plan_groups(int64_t n, int C, int G, const int64_t* ds, int nds) {
+  std::vector<int64_t> cuts;
+  cuts.push_back(0);
+  for (int i = 0; i < nds; ++i)
+    if (ds[i] > 0) cuts.push_back(ds[i]);
+  cuts.push_back(n);
+  std::vector<Span> out;
+  for (size_t i = 0; i + 1 < cuts.size(); ++i) {
+    const int64_t a = cuts[i], b = cuts[i + 1];
+    const bool doc = (i > 0) || (nds > 0 && ds[0] == 0);
+    for (int64_t t = a; t < b; t += (int64_t)G * C) {
+      const int64_t e = std::min<int64_t>(t + (int64_t)G * C, b);
+      out.push_back(Span{(int)t, (int)(e - t), doc && t == a});
+    }
+  }
+  return out;
+}
+
+template <int MODE>
+cudaError_t launch_gemm(ttt_mlp* h, GemmArgs& a, int ntiles, cudaStream_t st) {
+  if (ntiles <= 0) return cudaSuccess;
+  const int grid = std::max(1, std::min(h->num_sms, ntiles));
+  tc_gemm_kernel<MODE><<<grid, kGemmThreads, kGemmSmemBytes, st>>>(a);
+  return cudaGetLastError();
+}
+
+// Phase timing (only while profiling is enabled): an event pair per phase.
+struct PhaseTimer {
+  ttt_mlp* h;
+  cudaStream_t st;
+  int phase = -1;
+  cudaEvent_t a = nullptr;
+  void begin(int p) {
+    if (!h->profiling) return;
+    phase = p;
+    cudaEventCreate(&a);
+    cudaEventRecord(a, st);
+  }
+  void end() {
+    if (!h->profiling || phase < 0) return;
+    cudaEvent_t b;
+    cudaEventCreate(&b);
+    cudaEventRecord(b, st);
+    h->recs.push_back(ttt_mlp::Rec{phase, a, b});
+    phase = -1;
+  }
+};
+
+int* next_counter(ttt_mlp* h, cudaStream_t st) {
+  if (h->counter_next >= kCtrlInts) {
+    cudaMemsetAsync(h->ctrl + kCounterBase, 0, (kCtrlInts - kCounterBase) * sizeof(int), st);
+    h->counter_next = kCounterBase;
+  }
+  return h->ctrl + h->counter_next++;
+}
+
+ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_t n,
+                      const std::vector<Span>& groups, void* o, cudaStream_t st) {
+  const ttt_mlp_config& c = h->cfg;
+  const int d = c.d, f = c.f;
+  std::string why;
+  CUtensorMap map_x, map_u, map_za, map_zb, map_vmn, map_zmn;
+  if (!make_map(&map_x, x, d, n, d, 64, 128, &why) ||
+      !make_map(&map_u, h->U, d, n, d, 64, 128, &why) ||
+      !make_map(&map_za, h->Z, f, n, f, 64, 128, &why) ||
+      !make_map(&map_zb, h->Z, f, n, f, 64, 256, &why) ||
+      !make_map(&map_vmn, h->V, d, n, d, 64, 64, &why) ||
+      !make_map(&map_zmn, h->Z, f, n, f, 64, 64, &why))
+    return fail(h, TTT_ECUDA, why);
+
+  // fresh tile counters for this call
+  TTT_CK(h, cudaMemsetAsync(h->ctrl + kCounterBase, 0, (kCtrlInts - kCounterBase) * sizeof(int), st));
+  h->counter_next = kCounterBase;
+
+  PhaseTimer pt{h, st};
+  h->prof_calls++;
+  // chunk-local Conv1D target source U, wave by wave (<= kMaxSpans groups each)
+  pt.begin(0);
+  for (size_t w0 = 0; w0 < groups.size(); w0 += kMaxSpans) {
+    const size_t w1 = std::min(groups.size(), w0 + kMaxSpans);
+    SpanList sl{};
+    sl.n = (int)(w1 - w0);
+    sl.chunk = c.chunk;
+    for (size_t i = w0; i < w1; ++i) {
+      sl.start[i - w0] = groups[i].start;
+      sl.len[i - w0] = groups[i].len;
+    }
+    const long long cnt = (long long)(groups[w1 - 1].start + groups[w1 - 1].len - groups[w0].start) * (d / 8);
+    conv_target_kernel<__nv_bfloat16, __nv_bfloat16><<<grid_for(cnt, 256), 256, 0, st>>>(
+        (const __nv_bfloat16*)x0, (const __nv_bfloat16*)h->conv, (__nv_bfloat16*)h->U, d, c.conv_k, sl);
+    TTT_CK_LAUNCH(h);
+    h->prof_launches++;
+  }
+  pt.end();
+
+  GemmArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.n_rows = (int)n;
+  a.d = d;
+  a.f = f;
+  a.chunk = c.chunk;
+  a.err = h->ctrl;
+  a.s_pad = h->s_pad;
+
+  // Z = SiLU(X Wg^T) (.) (X Wu^T) for every token of the call (W-independent)
+  a.map[0] = map_x;
+  a.map[1] = h->map_wg;
+  a.map[2] = h->map_wu;
+  a.out0 = h->Z;
+  a.counter = next_counter(h, st);
+  pt.begin(1);
+  TTT_CK(h, launch_gemm<kSwiGLU>(h, a, ((int)n + kBM - 1) / kBM * ((f + kBM - 1) / kBM), st));
+  pt.end();
+  h->prof_launches++;
+
+  // V = eta * U W_target for every token
+  a.map[0] = map_u;
+  a.map[1] = h->map_wtT;
+  a.out0 = h->V;
+  a.alpha = c.eta;
+  a.counter = next_counter(h, st);
+  pt.begin(2);
+  TTT_CK(h, launch_gemm<kVProj>(h, a, ((int)n + kBM - 1) / kBM * ((d + kBN - 1) / kBN), st));
+  pt.end();
+  h->prof_launches++;
+
+  const size_t wsz = (size_t)d * f;
+  float* W = h->W + (size_t)doc * wsz;
+  for (size_t w0 = 0; w0 < groups.size(); w0 += (size_t)h->s_slots) {
+    const size_t w1 = std::min(groups.size(), w0 + (size_t)h->s_slots);
+    // intra-group Gram blocks S_g = mask(Z_g Z_g^T) of this wave
+    GemmArgs s;
+    std::memset(&s, 0, sizeof s);
+    s.n_rows = (int)n;
+    s.d = d;
+    s.f = f;
+    s.chunk = c.chunk;
+    s.err = h->ctrl;
+    s.s_pad = h->s_pad;
+    s.n_groups = (int)(w1 - w0);
+    for (size_t i = w0; i < w1; ++i) {
+      s.g_start[i - w0] = groups[i].start;
+      s.g_len[i - w0] = groups[i].len;
+    }
+    s.map[0] = map_za;
+    s.map[1] = map_zb;
+    s.out0 = h->S;
+    s.counter = next_counter(h, st);
+    const int per = ((h->s_pad + kBM - 1) / kBM) * ((h->s_pad + kBN - 1) / kBN);
+    if (h->G > 1) {
+      pt.begin(3);
+      TTT_CK(h, launch_gemm<kSGram>(h, s, s.n_groups * per, st));
+      pt.end();
+      h->prof_launches++;
+    }
+    pt.begin(4);
+
+    for (size_t i = w0; i < w1; ++i) {
+      const Span& g = groups[i];
+      if (!g.reset && h->wb_owner != doc) {
+        to_bf16_kernel<<<grid_for((long long)wsz, 256), 256, 0, st>>>(W, h->Wb[h->wb_cur], (long long)wsz);
+        TTT_CK_LAUNCH(h);
+        h->prof_launches++;
+        h->wb_owner = doc;
+      }
+      GemmArgs& q = a;
+      q.map[0] = map_za;
+      q.map[1] = g.reset ? h->map_w0 : h->map_wb[h->wb_cur];
+      q.map[2] = h->map_s;
+      q.map[3] = map_vmn;
+      const bool exact = (g.len % kBK == 0) || ((int64_t)g.start + g.len == n);
+      if (exact) {
+        q.map[4] = map_vmn;
+        q.map[5] = map_zmn;
+      } else {
+        const uint64_t ext = (uint64_t)g.start + (uint64_t)g.len;
+        if (!make_map(&q.map[4], h->V, d, ext, d, 64, 64, &why) ||
+            !make_map(&q.map[5], h->Z, f, ext, f, 64, 64, &why))
+          return fail(h, TTT_ECUDA, why);
+      }
+      q.out0 = o;
+      q.out1 = W;
+      q.out2 = h->Wb[h->wb_cur ^ 1];
+      q.in0 = h->w0;
+      q.g0 = g.start;
+      q.glen = g.len;
+      q.gslot = (int)(i - w0);
+      q.reset = g.reset ? 1 : 0;
+      q.counter = next_counter(h, st);
+      const int nt = ((g.len + kBM - 1) / kBM) * ((d + kBN - 1) / kBN) +
+                     ((d + kBM - 1) / kBM) * ((f + kBN - 1) / kBN);
+      TTT_CK(h, launch_gemm<kGroup>(h, q, nt, st));
+      h->prof_launches++;
+      h->prof_group_launches++;
+      h->wb_cur ^= 1;
+      h->wb_owner = doc;
+    }
+    pt.end();
+  }
+  return TTT_OK;
+}
+
+template <typename T>
+ttt_status forward_simt_t(ttt_mlp* h, int doc, const void* xv, const void* x0v, int64_t n,
+                          const std::vector<Span>& spans, void* ov, cudaStream_t st) {
+  const ttt_mlp_config& c = h->cfg;
+  const int d = c.d, f = c.f;
+  const T* x = (const T*)xv;
+  const T* x0 = (const T*)x0v;
+  T* o = (T*)ov;
+  float* Z = (float*)h->Z;
+  float* U = (float*)h->U;
+  float* V = (float*)h->V;
+  const size_t wsz = (size_t)d * f;
+  float* W = h->W + (size_t)doc * wsz;
+  const int nn = (int)n;
+
+  h->prof_calls++;
+  dim3 gz((f + 63) / 64, (nn + 63) / 64);
+  simt_swiglu_kernel<T><<<gz, 256, 0, st>>>(nn, f, d, x, (const T*)h->wg, (const T*)h->wu, Z);
+  TTT_CK_LAUNCH(h);
+  h->prof_launches++;
+  for (size_t w0 = 0; w0 < spans.size(); w0 += kMaxSpans) {
+    const size_t w1 = std::min(spans.size(), w0 + kMaxSpans);
+    SpanList sl{};
+    sl.n = (int)(w1 - w0);
+    sl.chunk = c.chunk;
+    for (size_t i = w0; i < w1; ++i) {
+      sl.start[i - w0] = spans[i].start;
+      sl.len[i - w0] = spans[i].len;
+    }
+    const long long cnt = (long long)(spans[w1 - 1].start + spans[w1 - 1].len - spans[w0].start) * (d / 8);
+    conv_target_kernel<T, float><<<grid_for(cnt, 256), 256, 0, st>>>(x0, (const T*)h->conv, U, d, c.conv_k, sl);
+    TTT_CK_LAUNCH(h);
+    h->prof_launches++;
+  }
+  dim3 gv((d + 63) / 64, (nn + 63) / 64);
+  simt_gemm_kernel<float, T, float><<<gv, 256, 0, st>>>(nn, d, d, U, d, 1, (const T*)h->wt, d, 1, V, d, c.eta, 0.0f);
+  TTT_CK_LAUNCH(h);
+  h->prof_launches++;
+  for (const Span& s : spans) {
+    if (s.reset) {
+      to_f32_kernel<T><<<grid_for((long long)wsz, 256), 256, 0, st>>>((const T*)h->w0, W, (long long)wsz);
+      TTT_CK_LAUNCH(h);
+      h->prof_launches++;
+    }
+    // apply: O_c = Z_c W^T with the state before this chunk's update
+    dim3 ga((d + 63) / 64, (s.len + 63) / 64);
+    simt_gemm_kernel<float, float, T><<<ga, 256, 0, st>>>(s.len, d, f, Z + (size_t)s.start * f, f, 1, W, 1, f,
+                                                          o + (size_t)s.start * d, d, 1.0f, 0.0f);
+    TTT_CK_LAUNCH(h);
+    // update: W += (eta V_c)^T Z_c
+    dim3 gu((f + 63) / 64, (d + 63) / 64);
+    simt_gemm_kernel<float, float, float><<<gu, 256, 0, st>>>(d, f, s.len, V + (size_t)s.start * d, 1, d,
+                                                              Z + (size_t)s.start * f, f, 1, W, f, 1.0f, 1.0f);
+    TTT_CK_LAUNCH(h);
+    h->prof_launches += 2;
+  }
+  h->wb_owner = -1;
+  return TTT_OK;
+}
+
+ttt_status check_handle(const ttt_mlp* h) {
+  if (!h) return fail(nullptr, TTT_EINVAL, "handle is NULL");
+  return TTT_OK;
+}
+
+ttt_status validate_call(ttt_mlp* h, int doc, const void* x, const void* x0, int64_t n,
+                         const int64_t* ds, int nds, const void* o) {
+  const ttt_mlp_config& c = h->cfg;
+  if (doc < 0 || doc >= c.n_docs) return fail(h, TTT_EINVAL, "doc slot out of range");
+  if (n < 0 || n > c.max_tokens) return fail(h, TTT_EINVAL, "n_tokens must be in 0..max_tokens");
+  if (nds < 0 || (nds > 0 && !ds)) return fail(h, TTT_EINVAL, "doc_starts is NULL but n_doc_starts > 0");
+  for (int i = 0; i < nds; ++i) {
+    if (ds[i] < 0 || ds[i] >= std::max<int64_t>(n, 1) || (n == 0))
+      return fail(h, TTT_EINVAL, "document starts must lie in [0, n_tokens)");
+    if (i > 0 && ds[i] <= ds[i - 1]) return fail(h, TTT_EINVAL, "document starts must be strictly increasing");
+  }
+  if (n == 0) return TTT_OK;
+  if (!x || !x0 || !o) return fail(h, TTT_EINVAL, "x, x0 and o must be non-NULL");
+  if (!aligned16(x) || !aligned16(x0) || !aligned16(o)) return fail(h, TTT_EINVAL, "x, x0 and o must be 16-byte aligned");
+  const size_t bytes = (size_t)n * c.d * (c.act_dtype == TTT_BF16 ? 2 : 4);
+  auto overlap = [&](const void* p, const void* q) {
+    const uintptr_t a0 = (uintptr_t)p, b0 = (uintptr_t)q;
+    return a0 < b0 + bytes && b0 < a0 + bytes;
+  };
+  if (overlap(o, x) || overlap(o, x0)) return fail(h, TTT_EINVAL, "o must not overlap x or x0");
+  return TTT_OK;
+}
+
+ttt_status forward_impl(ttt_mlp* h, int doc, const void* x, const void* x0, int64_t n,
+                        const int64_t* ds, int nds, void* o, cudaStream_t st) {
+  if (n == 0) return TTT_OK;
+  if (h->tc) {
+    std::vector<Span> groups = plan_groups(n, h->cfg.chunk, h->G, ds, nds);
+    return forward_tc(h, doc, x, x0, n, groups, o, st);
+  }
+  std::vector<Span> spans = plan_groups(n, h->cfg.chunk, 1, ds, nds);
+  if (h->cfg.act_dtype == TTT_BF16)
+    return forward_simt_t<__nv_bfloat16>(h, doc, x, x0, n, spans, o, st);
+  return forward_simt_t<float>(h, doc, x, x0, n, spans, o, st);
+}
+
+ttt_status reset_slot(ttt_mlp* h, int doc, cudaStream_t st) {
+  const size_t wsz = (size_t)h->cfg.d * h->cfg.f;
+  float* W = h->W + (size_t)doc * wsz;
+  if (h->cfg.act_dtype == TTT_BF16)
+    to_f32_kernel<__nv_bfloat16><<<grid_for((long long)wsz, 256), 256, 0, st>>>((const __nv_bfloat16*)h->w0, W, (long long)wsz);
+  else
+    to_f32_kernel<float><<<grid_for((long long)wsz, 256), 256, 0, st>>>((const float*)h->w0, W, (long long)wsz);
+  TTT_CK_LAUNCH(h);
+  if (h->wb_owner == doc) h->wb_owner = -1;
+  return TTT_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+size_t ttt_mlp_workspace_bytes(const ttt_mlp_config* cfg) {
+  std::string why;
+  if (!config_ok(cfg, &why)) return 0;
+  size_t b = make_layout(*cfg, false).total;
+  if (tc_shape_ok(*cfg)) b = std::max(b, make_layout(*cfg, true).total);
+  return b;
+}
+
+ttt_status ttt_mlp_create(const ttt_mlp_config* cfg, const void* w_gate, const void* w_up,
+                          const void* w_down0, const void* conv_w, const void* w_target,
+                          void* workspace, size_t workspace_bytes, void* stream, ttt_mlp** out) {
+  if (fault_injected("create")) return fail(nullptr, TTT_EFAULT_INJECTED, "fault injected: create");
+  if (!out) return fail(nullptr, TTT_EINVAL, "out is NULL");
+  *out = nullptr;
+  std::string why;
+  if (!config_ok(cfg, &why)) return fail(nullptr, TTT_EINVAL, why);
+  const void* ptrs[5] = {w_gate, w_up, w_down0, conv_w, w_target};
+  for (const void* p : ptrs) {
+    if (!p) return fail(nullptr, TTT_EINVAL, "weight pointers must be non-NULL");
+    if (!aligned16(p)) return fail(nullptr, TTT_EINVAL, "weight pointers must be 16-byte aligned");
+  }
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(nullptr, TTT_EINVAL, "workspace must be non-NULL and 256-byte aligned");
+  const bool tc = tc_shape_ok(*cfg) && !force_simt();
+  const Layout l = make_layout(*cfg, tc);
+  if (workspace_bytes < l.total) return fail(nullptr, TTT_EINVAL, "workspace is smaller than ttt_mlp_workspace_bytes()");
+
+  ttt_mlp* h = new ttt_mlp();
+  h->cfg = *cfg;
+  h->wg = w_gate;
+  h->wu = w_up;
+  h->w0 = w_down0;
+  h->conv = conv_w;
+  h->wt = w_target;
+  h->ws = (uint8_t*)workspace;
+  h->ws_bytes = workspace_bytes;
+  h->tc = tc;
+  h->G = l.G;
+  h->L = l.L;
+  h->s_pad = l.s_pad;
+  h->s_slots = l.s_slots;
+  h->ctrl = (int*)(h->ws + l.ctrl);
+  h->W = (float*)(h->ws + l.W);
+  h->Wb[0] = (__nv_bfloat16*)(h->ws + l.Wb0);
+  h->Wb[1] = (__nv_bfloat16*)(h->ws + l.Wb1);
+  h->WtT = (__nv_bfloat16*)(h->ws + l.WtT);
+  h->Z = h->ws + l.Z;
+  h->U = h->ws + l.U;
+  h->V = h->ws + l.V;
+  h->S = (__nv_bfloat16*)(h->ws + l.S);
+  h->xs = h->ws + l.xs;
+  h->x0s = h->ws + l.x0s;
+  h->os = h->ws + l.os;
+  h->counter_next = kCounterBase;
+  h->wb_owner = -1;
+  h->wb_cur = 0;
+  cudaStream_t st = (cudaStream_t)stream;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    std::string m = std::string("cudaGetDevice/attribute: ") + cudaGetErrorString(e);
+    delete h;
+    return fail(nullptr, TTT_ECUDA, m);
+  }
+  auto bail = [&](ttt_status s, const std::string& m) {
+    delete h;
+    return fail(nullptr, s, m);
+  };
+  if (tc) {
+    const int d = cfg->d, f = cfg->f;
+    if (!make_map(&h->map_wg, w_gate, d, f, d, 64, 128, &why) ||
+        !make_map(&h->map_wu, w_up, d, f, d, 64, 128, &why) ||
+        !make_map(&h->map_wtT, h->WtT, d, d, d, 64, 256, &why) ||
+        !make_map(&h->map_s, h->S, h->s_pad, (uint64_t)h->s_slots * h->s_pad, h->s_pad, 64, 128, &why) ||
+        !make_map(&h->map_w0, w_down0, f, d, f, 64, 256, &why) ||
+        !make_map(&h->map_wb[0], h->Wb[0], f, d, f, 64, 256, &why) ||
+        !make_map(&h->map_wb[1], h->Wb[1], f, d, f, 64, 256, &why))
+      return bail(TTT_ECUDA, why);
+    const void* kfn[4] = {(const void*)tc_gemm_kernel<kSwiGLU>, (const void*)tc_gemm_kernel<kVProj>,
+                          (const void*)tc_gemm_kernel<kSGram>, (const void*)tc_gemm_kernel<kGroup>};
+    for (const void* k : kfn) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+      if (e != cudaSuccess) return bail(TTT_ECUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+    }
+    dim3 tb(32, 8), tg((d + 31) / 32, (d + 31) / 32);
+    transpose_kernel<__nv_bfloat16><<<tg, tb, 0, st>>>((const __nv_bfloat16*)w_target, h->WtT, d, d);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return bail(TTT_ECUDA, std::string("transpose launch: ") + cudaGetErrorString(e));
+  }
+  e = cudaMemsetAsync(h->ctrl, 0, kCtrlInts * sizeof(int), st);
+  if (e != cudaSuccess) return bail(TTT_ECUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+  for (int s = 0; s < cfg->n_docs; ++s) {
+    if (reset_slot(h, s, st) != TTT_OK) {
+      std::string m = h->err;
+      delete h;
+      return fail(nullptr, TTT_ECUDA, m);
+    }
+  }
+  *out = h;
+  return TTT_OK;
+}
+
+ttt_status ttt_mlp_forward_chunks(ttt_mlp* h, int32_t doc, const void* x, const void* x0,
+                                  int64_t n_tokens, const int64_t* doc_starts,
+                                  int32_t n_doc_starts, void* o, void* stream) {
+  if (check_handle(h)) return TTT_EINVAL;
+  if (fault_injected("forward")) return fail(h, TTT_EFAULT_INJECTED, "fault injected: forward");
+  ttt_status s = validate_call(h, doc, x, x0, n_tokens, doc_starts, n_doc_starts, o);
+  if (s != TTT_OK) return s;
+  return forward_impl(h, doc, x, x0, n_tokens, doc_starts, n_doc_starts, o, (cudaStream_t)stream);
+}
+
+ttt_status ttt_mlp_forward_chunks_host(ttt_mlp* h, int32_t doc, const void* x_host,
+                                       const void* x0_host, int64_t n_tokens,
+                                       const int64_t* doc_starts, int32_t n_doc_starts,
+                                       void* o_host, void* stream) {
+  if (check_handle(h)) return TTT_EINVAL;
+  if (fault_injected("forward")) return fail(h, TTT_EFAULT_INJECTED, "fault injected: forward");
+  if (n_tokens > 0 && (!x_host || !x0_host || !o_host))
+    return fail(h, TTT_EINVAL, "host buffers must be non-NULL");
+  ttt_status s = validate_call(h, doc, h->xs, h->x0s, n_tokens, doc_starts, n_doc_starts, h->os);
+  if (s != TTT_OK || n_tokens == 0) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t bytes = (size_t)n_tokens * h->cfg.d * (h->cfg.act_dtype == TTT_BF16 ? 2 : 4);
+  TTT_CK(h, cudaMemcpyAsync(h->xs, x_host, bytes, cudaMemcpyHostToDevice, st));
+  const void* x0d = h->xs;
+  if (x0_host != x_host) {
+    TTT_CK(h, cudaMemcpyAsync(h->x0s, x0_host, bytes, cudaMemcpyHostToDevice, st));
+    x0d = h->x0s;
+  }
+  s = forward_impl(h, doc, h->xs, x0d, n_tokens, doc_starts, n_doc_starts, h->os, st);
+  if (s != TTT_OK) return s;
+  TTT_CK(h, cudaMemcpyAsync(o_host, h->os, bytes, cudaMemcpyDeviceToHost, st));
+  return TTT_OK;
+}
+
+ttt_status ttt_mlp_reset(ttt_mlp* h, int32_t doc, void* stream) {
+  if (check_handle(h)) return TTT_EINVAL;
+  if (fault_injected("reset")) return fail(h, TTT_EFAULT_INJECTED, "fault injected: reset");
+  if (doc < -1 || doc >= h->cfg.n_docs) return fail(h, TTT_EINVAL, "doc slot out of range");
+  for (int s = (doc < 0 ? 0 : doc); s < (doc < 0 ? h->cfg.n_docs : doc + 1); ++s) {
+    ttt_status r = reset_slot(h, s, (cudaStream_t)stream);
+    if (r != TTT_OK) return r;
+  }
+  return TTT_OK;
+}
+
+ttt_status ttt_mlp_get_fast_weight(ttt_mlp* h, int32_t doc, float* dst, void* stream) {
+  if (check_handle(h)) return TTT_EINVAL;
+  if (fault_injected("get")) return fail(h, TTT_EFAULT_INJECTED, "fault injected: get");
+  if (doc < 0 || doc >= h->cfg.n_docs) return fail(h, TTT_EINVAL, "doc slot out of range");
+  if (!dst) return fail(h, TTT_EINVAL, "dst is NULL");
+  const size_t wsz = (size_t)h->cfg.d * h->cfg.f;
+  TTT_CK(h, cudaMemcpyAsync(dst, h->W + (size_t)doc * wsz, wsz * 4, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+  return TTT_OK;
+}
+
+ttt_status ttt_mlp_set_fast_weight(ttt_mlp* h, int32_t doc, const float* src, void* stream) {
+  if (check_handle(h)) return TTT_EINVAL;
+  if (fault_injected("set")) return fail(h, TTT_EFAULT_INJECTED, "fault injected: set");
+  if (doc < 0 || doc >= h->cfg.n_docs) return fail(h, TTT_EINVAL, "doc slot out of range");
+  if (!src) return fail(h, TTT_EINVAL, "src is NULL");
+  const size_t wsz = (size_t)h->cfg.d * h->cfg.f;
+  TTT_CK(h, cudaMemcpyAsync(h->W + (size_t)doc * wsz, src, wsz * 4, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+  if (h->wb_owner == doc) h->wb_owner = -1;
+  return TTT_OK;
+}
+
+ttt_status ttt_mlp_check(ttt_mlp* h, void* stream) {
+  if (check_handle(h)) return TTT_EINVAL;
+  if (fault_injected("check")) return fail(h, TTT_EFAULT_INJECTED, "fault injected: check");
+  cudaStream_t st = (cudaStream_t)stream;
+  TTT_CK(h, cudaStreamSynchronize(st));
+  int word = 0;
+  TTT_CK(h, cudaMemcpy(&word, h->ctrl, sizeof(int), cudaMemcpyDeviceToHost));
+  if (word != 0) {
+    TTT_CK(h, cudaMemset(h->ctrl, 0, sizeof(int)));
+    char buf[96];
+    std::snprintf(buf, sizeof buf, "an in-kernel wait ran out (code %d)", word);
+    return fail(h, TTT_ETIMEOUT, buf);
+  }
+  return TTT_OK;
+}
+
+ttt_status ttt_mlp_destroy(ttt_mlp* h) {
+  if (!h) return fail(nullptr, TTT_EINVAL, "handle is NULL");
+  ttt_mlp_profile_enable(h, 0);
+  delete h;
+  return TTT_OK;
+}
+
+const char* ttt_mlp_last_error(const ttt_mlp* h) { return h ? h->err.c_str() : g_err.c_str(); }
+
+ttt_status ttt_mlp_intermediates(const ttt_mlp* h, const void** z, const void** v, int32_t* dtype) {
+  if (!h || !z || !v || !dtype) return fail(nullptr, TTT_EINVAL, "ttt_mlp_intermediates: NULL argument");
+  *z = h->Z;
+  *v = h->V;
+  *dtype = h->tc ? TTT_BF16 : TTT_F32;
+  return TTT_OK;
+}
+
+ttt_status ttt_mlp_profile_enable(ttt_mlp* h, int32_t enable) {
+  if (check_handle(h)) return TTT_EINVAL;
+  for (auto& r : h->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  h->recs.clear();
+  h->prof_calls = h->prof_group_launches = h->prof_launches = 0;
+  h->profiling = enable != 0;
+  return TTT_OK;
+}
+
+ttt_status ttt_mlp_profile_read(ttt_mlp* h, float* ms, int64_t* counts) {
+  if (check_handle(h)) return TTT_EINVAL;
+  if (!ms || !counts) return fail(h, TTT_EINVAL, "ttt_mlp_profile_read: NULL argument");
+  for (int i = 0; i < 5; ++i) ms[i] = 0.0f;
+  for (auto& r : h->recs) {
+    TTT_CK(h, cudaEventSynchronize(r.b));
+    float t = 0.0f;
+    TTT_CK(h, cudaEventElapsedTime(&t, r.a, r.b));
+    if (r.phase >= 0 && r.phase < 5) ms[r.phase] += t;
+  }
+  counts[0] = h->prof_calls;
+  counts[1] = h->prof_group_launches;
+  counts[2] = h->prof_launches;
+  return TTT_OK;
+}
+
+const char* ttt_mlp_path(const ttt_mlp* h) { return (h && h->tc) ? "tcgen05" : "simt"; }
+
+ttt_status ttt_rmsnorm(const float* hs, void* x, int64_t n, int32_t d, float eps, int32_t out_dtype,
+                       void* stream) {
+  if (n < 0 || d < 1 || (n > 0 && (!hs || !x)) || (out_dtype != TTT_F32 && out_dtype != TTT_BF16))
+    return fail(nullptr, TTT_EINVAL, "ttt_rmsnorm: bad arguments");
+  if (n == 0) return TTT_OK;
+  if (n > (int64_t(1) << 31) - 1) return fail(nullptr, TTT_EUNSUPPORTED, "ttt_rmsnorm: too many rows");
+  cudaStream_t st = (cudaStream_t)stream;
+  if (out_dtype == TTT_BF16)
+    rmsnorm_kernel<__nv_bfloat16><<<(unsigned)n, 256, 0, st>>>(hs, (__nv_bfloat16*)x, d, eps);
+  else
+    rmsnorm_kernel<float><<<(unsigned)n, 256, 0, st>>>(hs, (float*)x, d, eps);
+  TTT_CK(nullptr, cudaGetLastError());
+  return TTT_OK;
+}
+
+ttt_status ttt_residual_add(float* hs, const void* o, int64_t n, int32_t d, int32_t o_dtype, void* stream) {
+  if (n < 0 || d < 1 || (n > 0 && (!hs || !o)) || (o_dtype != TTT_F32 && o_dtype != TTT_BF16))
+    return fail(nullptr, TTT_EINVAL, "ttt_residual_add: bad arguments");
+  if (n == 0) return TTT_OK;
+  const long long cnt = n * (long long)d;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (o_dtype == TTT_BF16)
+    residual_add_kernel<__nv_bfloat16><<<grid_for(cnt, 256), 256, 0, st>>>(hs, (const __nv_bfloat16*)o, cnt);
+  else
+    residual_add_kernel<float><<<grid_for(cnt, 256), 256, 0, st>>>(hs, (const float*)o, cnt);
+  TTT_CK(nullptr, cudaGetLastError());
+  return TTT_OK;
+}
+
+}  // extern "C"

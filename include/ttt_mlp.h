@@ -1,0 +1,175 @@
+/*
+ * ttt_mlp.h -- C ABI of the B300 (sm_103a) In-Place TTT fast-weight MLP layer.
+ *
+ * What the layer computes (sources: "In-Place Test-Time Training",
+ * paperlayer.ai summary of arXiv 2604.06169v1, section 3 "In-Place Adaptation",
+ * "Chunk-Wise Updates", "LM-Aligned Objective" and appendix B "Context Parallel
+ * Algorithm"; iplexlaw.co.kr walkthrough of the same paper, sections 2-4 and 6):
+ *
+ *   The tokens of a call are cut into non-overlapping chunks of C tokens
+ *   (a document start restarts the chunking; the last chunk may be short).
+ *   For every chunk c, in order:
+ *     Z_c     = SiLU(X_c W_gate^T) (.) (X_c W_up^T)          gated intermediate
+ *     O_c     = Z_c W_c^T                                      apply (pre-update W)
+ *     U_c[t]  = sum_{j<k} conv[j] (.) X0_c[t+1+j]              zero past the chunk end
+ *     V_c     = U_c W_target                                   next-token target
+ *     W_{c+1} = W_c + eta V_c^T Z_c                            update
+ *   The fast weight W (= the MLP's down projection) starts at the frozen
+ *   W_down = W_0 and is reset to W_0 at every document start.
+ *
+ * Conventions shared by every call:
+ *   - Layouts are row-major.  W_gate, W_up: f x d; W_down (W_0): d x f;
+ *     conv: k x d; W_target: d x d given as in x out (V = U W_target);
+ *     X, X0, O: n x d (row = token); the fast weight W: d x f, always fp32.
+ *   - Activations and weights are fp32 (TTT_F32) or bf16 (TTT_BF16) as set by
+ *     ttt_mlp_config.act_dtype; O has the same dtype.
+ *   - Device memory is never allocated by the library.  The caller owns the
+ *     weights, the workspace and the per-call buffers; weights and workspace
+ *     are borrowed by the handle and must outlive it.  The handle owns only
+ *     host memory.  Pointers are device pointers unless named *_host.
+ *   - Every call is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and returns without synchronising, except where stated.
+ *   - No exception or abort crosses the ABI.  Arguments are checked on the
+ *     host before anything is enqueued; a call that fails its checks changes
+ *     no state and returns TTT_EINVAL or TTT_EUNSUPPORTED.  CUDA errors map
+ *     to TTT_ECUDA.  ttt_mlp_last_error() gives the text of the last failure.
+ *   - Kernels never hang: every in-kernel wait is bounded.  A wait that runs
+ *     out records a code in the workspace's error word; ttt_mlp_check()
+ *     reports it as TTT_ETIMEOUT.
+ *   - Setting the environment variable TTT_FAULT to one of
+ *     create|forward|reset|get|set|check makes that call fail with
+ *     TTT_EFAULT_INJECTED before it does anything (host-side fault injection).
+ */
+#ifndef TTT_MLP_H
+#define TTT_MLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TTT_OK = 0,
+  TTT_EINVAL = 1,           /* a bad argument (null pointer, size, alignment, order) */
+  TTT_EUNSUPPORTED = 2,     /* valid but outside what this build supports */
+  TTT_ECUDA = 3,            /* a CUDA runtime/driver call failed */
+  TTT_ETIMEOUT = 4,         /* a bounded in-kernel wait ran out (see ttt_mlp_check) */
+  TTT_EFAULT_INJECTED = 5   /* TTT_FAULT named this call */
+} ttt_status;
+
+typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
+
+typedef struct {
+  int32_t d;            /* model width; >= 8 and a multiple of 8 */
+  int32_t f;            /* MLP intermediate width; >= 8 and a multiple of 8 */
+  int32_t chunk;        /* C, tokens per chunk; 1..1024 */
+  int32_t conv_k;       /* depthwise Conv1D taps k; 1..8 */
+  int32_t n_docs;       /* document slots; each has its own fast weight; >= 1 */
+  float eta;            /* fast-weight learning rate */
+  int32_t act_dtype;    /* ttt_dtype of X, X0, O and all weights */
+  int64_t max_tokens;   /* largest n_tokens of one forward call; >= 1 */
+} ttt_mlp_config;
+
+typedef struct ttt_mlp ttt_mlp; /* opaque handle */
+
+/* Bytes of device workspace a handle with this configuration needs (0 if the
+ * configuration is invalid).  The workspace holds the n_docs fast weights,
+ * their bf16 operand copies, the per-call intermediates (Z, U, V, the
+ * intra-group Gram blocks), host-staging buffers and a small control area.
+ * Host only; no CUDA call. */
+size_t ttt_mlp_workspace_bytes(const ttt_mlp_config* cfg);
+
+/* Create a handle.  The five weight pointers are device buffers of act_dtype
+ * in the layouts above; they must be 16-byte aligned and stay valid and
+ * unchanged for the handle's lifetime (W_0 is read again at every reset).
+ * `workspace` is a device buffer of at least ttt_mlp_workspace_bytes(cfg)
+ * bytes, 256-byte aligned.  Enqueues: every slot's W <- W_0 and a transposed
+ * copy of W_target.  On success *out receives the handle. */
+ttt_status ttt_mlp_create(const ttt_mlp_config* cfg, const void* w_gate, const void* w_up,
+                          const void* w_down0, const void* conv_w, const void* w_target,
+                          void* workspace, size_t workspace_bytes, void* stream,
+                          ttt_mlp** out);
+
+/* Run the layer over n_tokens tokens of document slot `doc`, continuing that
+ * slot's fast weight.  x, x0: n_tokens x d device buffers (x0 may equal x);
+ * o: n_tokens x d output (must not overlap x or x0).  doc_starts: host array
+ * of n_doc_starts strictly increasing offsets in [0, n_tokens) at which a new
+ * document begins (W <- W_0 there); may be NULL when n_doc_starts == 0.  The
+ * call always starts a fresh chunk at token 0; its trailing partial chunk is
+ * processed as a short chunk, and the slot's W afterwards is the state after
+ * the last chunk.  0 <= n_tokens <= max_tokens. */
+ttt_status ttt_mlp_forward_chunks(ttt_mlp* h, int32_t doc, const void* x, const void* x0,
+                                  int64_t n_tokens, const int64_t* doc_starts,
+                                  int32_t n_doc_starts, void* o, void* stream);
+
+/* The same call with host buffers: x_host / x0_host are copied to device
+ * staging inside the workspace, the layer runs, and O is copied back into
+ * o_host, all on `stream`.  Pinned (page-locked) host buffers make the copies
+ * asynchronous; the call returns once they are enqueued, so the caller must
+ * synchronise `stream` before reading o_host or reusing x_host. */
+ttt_status ttt_mlp_forward_chunks_host(ttt_mlp* h, int32_t doc, const void* x_host,
+                                       const void* x0_host, int64_t n_tokens,
+                                       const int64_t* doc_starts, int32_t n_doc_starts,
+                                       void* o_host, void* stream);
+
+/* Reset slot `doc` (or every slot when doc == -1) to W <- W_0 (document
+ * boundary, appendix B of the summary page). */
+ttt_status ttt_mlp_reset(ttt_mlp* h, int32_t doc, void* stream);
+
+/* Copy slot `doc`'s fp32 fast weight (d x f) to / from a device buffer. */
+ttt_status ttt_mlp_get_fast_weight(ttt_mlp* h, int32_t doc, float* dst, void* stream);
+ttt_status ttt_mlp_set_fast_weight(ttt_mlp* h, int32_t doc, const float* src, void* stream);
+
+/* Synchronise `stream` and read the workspace's error word: TTT_OK, or
+ * TTT_ETIMEOUT if an in-kernel wait ran out since the last check (the word is
+ * cleared), or TTT_ECUDA on an asynchronous CUDA error. */
+ttt_status ttt_mlp_check(ttt_mlp* h, void* stream);
+
+/* Free the handle (host memory only; device memory stays the caller's). */
+ttt_status ttt_mlp_destroy(ttt_mlp* h);
+
+/* Text of the last failure on this handle ("" if none); with h == NULL, of
+ * the last failure of a call that had no handle.  Valid until the next call. */
+const char* ttt_mlp_last_error(const ttt_mlp* h);
+
+/* Device pointers, inside the workspace, of the last forward call's Z
+ * (n x f) and eta-scaled target V (n x d, i.e. eta * U W_target), and their
+ * element type (*dtype: TTT_BF16 on the tcgen05 path, TTT_F32 on the SIMT
+ * path).  For inspection and tests; valid until the next forward call. */
+ttt_status ttt_mlp_intermediates(const ttt_mlp* h, const void** z, const void** v,
+                                 int32_t* dtype);
+
+/* Phase timing for benchmarks.  While enabled, every forward call records
+ * CUDA events on its stream at the boundaries of its phases (no extra
+ * synchronisation).  ttt_mlp_profile_read synchronises those events and
+ * returns, summed over the calls since profiling was (re-)enabled,
+ * ms[0] Conv1D target source, ms[1] SwiGLU producer, ms[2] target projection,
+ * ms[3] intra-group Gram blocks, ms[4] fused apply+update group kernels
+ * (ms must hold 5 floats), and counts[0] forward calls, counts[1] group
+ * kernel launches, counts[2] all kernel launches of the library (counts must
+ * hold 3 int64).  Enabling clears what was recorded. */
+ttt_status ttt_mlp_profile_enable(ttt_mlp* h, int32_t enable);
+ttt_status ttt_mlp_profile_read(ttt_mlp* h, float* ms, int64_t* counts);
+
+/* Which kernel family runs a forward call of this handle: "tcgen05" (bf16
+ * tensor-core path) or "simt" (fp32 FFMA path).  Host only. */
+const char* ttt_mlp_path(const ttt_mlp* h);
+
+/* ---- residual-stack glue (pre-norm blocks h <- h + MLP_TTT(RMSNorm(h))) ---- */
+
+/* x[t] = RMSNorm(h[t]) = h[t] / sqrt(mean(h[t]^2) + eps), unit gain, cast to
+ * out_dtype.  h: n x d fp32; x: n x d.  Returns TTT_EINVAL on bad sizes. */
+ttt_status ttt_rmsnorm(const float* h, void* x, int64_t n, int32_t d, float eps,
+                       int32_t out_dtype, void* stream);
+
+/* h += o elementwise; h: n x d fp32, o: n x d of o_dtype. */
+ttt_status ttt_residual_add(float* h, const void* o, int64_t n, int32_t d, int32_t o_dtype,
+                            void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TTT_MLP_H */

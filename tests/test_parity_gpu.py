@@ -1,0 +1,254 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU fp64 oracle on
+the same seeded inputs.
+
+Tolerances (relative Frobenius error ||gpu - oracle|| / ||oracle||):
+  * fp32 activations (FFMA path, no TF32):        1e-5 on O and on final W
+  * bf16 activations / fp32 accumulation and W:    1e-2 on O and on final W
+The bf16 path also reports the error of the TTT part alone, O - Z W_0^T, which
+the static part would otherwise dominate; it must stay within 5e-2 (the bf16
+roundings of Z, V, the Gram block and the W operand copy are each ~2^-9
+relative; measured values are far below this bound).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.ttt_oracle as orc
+from ttt_inputs import make_layer
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32 = 1e-5
+TOL_BF16 = 1e-2
+TOL_TTT_PART = 5e-2
+
+
+def _rel(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def _dev(a, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return t.to(device="cuda", dtype=dtype)
+
+
+def _host(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def _make_gpu_layer(cfg, n_docs=1, max_tokens=None, dtype=None):
+    from chunk_wise_weight_ttt_b300 import TTTMLP
+    dt = dtype or (torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32)
+    ws = [_dev(cfg[k], dt) for k in ("w_gate", "w_up", "w_down0", "conv_w", "w_target")]
+    layer = TTTMLP(*ws, chunk=cfg["chunk"], eta=cfg["eta"], n_docs=n_docs,
+                   max_tokens=max_tokens or cfg["T"])
+    return layer, dt
+
+
+def _oracle(cfg, eta=None, doc_starts=None, x=None, w_init=None):
+    x = cfg["x"] if x is None else x
+    return orc.ttt_layer(x, x, cfg["w_gate"], cfg["w_up"], cfg["w_down0"], cfg["conv_w"],
+                         cfg["w_target"], cfg["eta"] if eta is None else eta, cfg["chunk"],
+                         cfg["doc_starts"] if doc_starts is None else doc_starts, w_init=w_init)
+
+
+def _check_layer(cfg, tol, ttt_tol=None, force_simt=False, expect_path=None):
+    if force_simt:
+        os.environ["TTT_FORCE_SIMT"] = "1"
+    try:
+        layer, dt = _make_gpu_layer(cfg)
+    finally:
+        os.environ.pop("TTT_FORCE_SIMT", None)
+    if expect_path:
+        assert layer.path == expect_path
+    x = _dev(cfg["x"], dt)
+    o = layer.forward(x, doc_starts=cfg["doc_starts"])
+    w = layer.get_fast_weight()
+    layer.check()
+    torch.cuda.synchronize()
+    o_ref, w_ref = _oracle(cfg)
+    eo, ew = _rel(_host(o), o_ref), _rel(_host(w), w_ref)
+    msg = f"O err {eo:.3e}  W err {ew:.3e}"
+    if ttt_tol is not None:
+        o_static, _ = _oracle(cfg, eta=0.0)
+        part_gpu, part_ref = _host(o) - o_static, o_ref - o_static
+        ep = _rel(part_gpu, part_ref)
+        frac = np.linalg.norm(part_ref) / np.linalg.norm(o_ref)
+        msg += f"  TTT-part err {ep:.3e} (TTT part is {frac:.1%} of O)"
+        if frac > 1e-6:  # a single chunk has no TTT part
+            assert ep <= ttt_tol, msg
+    print(msg)
+    assert eo <= tol and ew <= tol, msg
+    return layer
+
+
+# ------------------------------------------------------------------ fp32 path
+
+def test_tiny_fp32_config_full():
+    """d=64, f=256, T=1024, C=64, k=4, eta=0.01, fp32 -- the tiny configuration."""
+    cfg = make_layer(64, 256, 1024, 64, 4, 0.01, dtype="f32", seed=0, init="tiny")
+    _check_layer(cfg, TOL_F32, expect_path="simt")
+
+
+@pytest.mark.parametrize("T,C,k,starts", [(77, 16, 2, (0,)), (130, 7, 5, (0, 33, 100)),
+                                          (64, 64, 1, (0,)), (5, 8, 3, (0,))])
+def test_fp32_ragged(T, C, k, starts):
+    cfg = make_layer(16, 40, T, C, k, 0.05, dtype="f32", seed=T, init="tiny", doc_starts=starts)
+    _check_layer(cfg, TOL_F32, expect_path="simt")
+
+
+# ------------------------------------------------------------------ bf16 tcgen05 path
+
+def _bf16_cfg(d=256, f=512, T=1000, C=64, k=5, eta=0.5, seed=1, starts=(0,)):
+    return make_layer(d, f, T, C, k, eta, dtype="bf16", seed=seed, init="qwen", doc_starts=starts)
+
+
+def test_bf16_intermediates_z_and_v():
+    """Producer outputs on their own: Z (SwiGLU) and V = eta Conv1D(X0) W_target."""
+    cfg = _bf16_cfg(T=700, C=100)
+    layer, dt = _make_gpu_layer(cfg)
+    assert layer.path == "tcgen05"
+    x = _dev(cfg["x"], dt)
+    layer.forward(x, doc_starts=(0,))
+    layer.check()
+    z, v = layer.intermediates(cfg["T"])
+    z_ref = orc.swiglu_intermediate(cfg["x"], cfg["w_gate"], cfg["w_up"])
+    v_ref = np.concatenate([cfg["eta"] * orc.chunk_target(cfg["x"][s:e], cfg["conv_w"],
+                                                          cfg["w_target"])
+                            for s, e, _ in orc.chunk_spans(cfg["T"], cfg["chunk"], (0,))])
+    ez, ev = _rel(_host(z), z_ref), _rel(_host(v), v_ref)
+    print(f"Z err {ez:.3e}  V err {ev:.3e}")
+    assert ez < 8e-3 and ev < 8e-3
+
+
+@pytest.mark.parametrize("T,C,starts", [
+    (1000, 64, (0,)),            # 16 chunks; groups of 16 chunks, ragged tail
+    (1024, 256, (0,)),           # groups of 4 chunks
+    (1536, 512, (0,)),           # groups of 2 chunks
+    (2048, 1024, (0,)),          # one chunk per group
+    (900, 100, (0,)),            # chunk not a multiple of the 64-token K block
+    (1100, 128, (0, 300, 777)),  # document starts off the chunk grid
+    (300, 40, (0, 1, 2, 150)),   # one-token documents
+    (64, 256, (0,)),             # a single short chunk: static MLP
+])
+def test_bf16_tcgen05_parity(T, C, starts):
+    cfg = _bf16_cfg(T=T, C=C, starts=starts, seed=T + C)
+    _check_layer(cfg, TOL_BF16, ttt_tol=TOL_TTT_PART, expect_path="tcgen05")
+
+
+def test_bf16_simt_path_parity():
+    cfg = _bf16_cfg(T=500, C=64)
+    _check_layer(cfg, TOL_BF16, ttt_tol=TOL_TTT_PART, force_simt=True, expect_path="simt")
+
+
+def test_eta_zero_keeps_w0_bitwise():
+    cfg = _bf16_cfg(T=600, C=64, eta=0.0)
+    layer, dt = _make_gpu_layer(cfg)
+    layer.forward(_dev(cfg["x"], dt))
+    w = layer.get_fast_weight()
+    torch.cuda.synchronize()
+    assert np.array_equal(_host(w), np.float64(cfg["w_down0"]))
+
+
+def test_state_persists_across_calls_and_reset():
+    """Two calls (the second continues the document) equal the oracle run from
+    the first call's final state; reset() restores W_0 exactly."""
+    cfg = _bf16_cfg(T=1024, C=128)
+    layer, dt = _make_gpu_layer(cfg)
+    x = _dev(cfg["x"], dt)
+    o1 = layer.forward(x[:512], doc_starts=(0,))
+    o2 = layer.forward(x[512:], doc_starts=())
+    w = layer.get_fast_weight()
+    layer.check()
+    o_ref1, w_ref1 = _oracle(cfg, x=cfg["x"][:512], doc_starts=(0,))
+    o_ref2, w_ref2 = _oracle(cfg, x=cfg["x"][512:], doc_starts=(), w_init=w_ref1)
+    assert _rel(_host(o1), o_ref1) < TOL_BF16
+    assert _rel(_host(o2), o_ref2) < TOL_BF16
+    assert _rel(_host(w), w_ref2) < TOL_BF16
+    layer.reset()
+    assert np.array_equal(_host(layer.get_fast_weight()), np.float64(cfg["w_down0"]))
+
+
+def test_set_fast_weight_then_continue():
+    cfg = _bf16_cfg(T=512, C=64)
+    layer, dt = _make_gpu_layer(cfg)
+    rng = np.random.default_rng(5)
+    w_init = (np.float64(cfg["w_down0"]) + 0.01 * rng.standard_normal(cfg["w_down0"].shape))
+    layer.set_fast_weight(torch.from_numpy(w_init.astype(np.float32)).cuda())
+    o = layer.forward(_dev(cfg["x"], dt), doc_starts=())
+    w = layer.get_fast_weight()
+    o_ref, w_ref = _oracle(cfg, doc_starts=(), w_init=w_init.astype(np.float32))
+    assert _rel(_host(o), o_ref) < TOL_BF16 and _rel(_host(w), w_ref) < TOL_BF16
+
+
+def test_batch_slots_are_independent():
+    """Per-document fast weights: slot b equals document b run alone."""
+    cfgs = [make_layer(256, 512, 640, 64, 5, 0.05, dtype="bf16", seed=0, init="qwen",
+                       x_seed=1000 + b) for b in range(3)]
+    layer, dt = _make_gpu_layer(cfgs[0], n_docs=3)
+    outs = [layer.forward(_dev(c["x"], dt), doc=b) for b, c in enumerate(cfgs)]
+    for b, c in enumerate(cfgs):
+        o_ref, w_ref = _oracle(c)
+        assert _rel(_host(outs[b]), o_ref) < TOL_BF16
+        assert _rel(_host(layer.get_fast_weight(b)), w_ref) < TOL_BF16
+
+
+def test_host_buffer_entry_point():
+    cfg = _bf16_cfg(T=512, C=64)
+    layer, dt = _make_gpu_layer(cfg)
+    xh = _dev(cfg["x"], dt).cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    layer.forward_host(xh, out_host=oh, doc_starts=(0,))
+    torch.cuda.synchronize()
+    o_ref, _ = _oracle(cfg)
+    assert _rel(_host(oh), o_ref) < TOL_BF16
+
+
+def test_bad_call_arguments_change_nothing():
+    from chunk_wise_weight_ttt_b300 import TTTError
+    cfg = _bf16_cfg(T=256, C=64)
+    layer, dt = _make_gpu_layer(cfg)
+    x = _dev(cfg["x"], dt)
+    w_before = layer.get_fast_weight().clone()
+    with pytest.raises(TTTError, match="EINVAL"):
+        layer.forward(x, doc_starts=(0, 5, 5))          # not strictly increasing
+    with pytest.raises(TTTError, match="EINVAL"):
+        layer.forward(x, doc_starts=(0, 256))           # out of range
+    with pytest.raises(TTTError, match="EINVAL"):
+        layer.forward(x, doc=3)                         # no such slot
+    with pytest.raises(TTTError, match="EINVAL"):
+        layer.forward(x, out=x)                         # output overlaps input
+    assert torch.equal(layer.get_fast_weight(), w_before)
+    layer.check()
+
+
+def test_fault_injection_leaves_handle_usable(monkeypatch):
+    from chunk_wise_weight_ttt_b300 import TTTError
+    cfg = _bf16_cfg(T=256, C=64)
+    layer, dt = _make_gpu_layer(cfg)
+    x = _dev(cfg["x"], dt)
+    monkeypatch.setenv("TTT_FAULT", "forward")
+    with pytest.raises(TTTError, match="FAULT_INJECTED"):
+        layer.forward(x)
+    monkeypatch.delenv("TTT_FAULT")
+    o = layer.forward(x)
+    o_ref, _ = _oracle(cfg)
+    assert _rel(_host(o), o_ref) < TOL_BF16
+
+
+def test_rmsnorm_and_residual_glue():
+    from chunk_wise_weight_ttt_b300 import residual_add, rmsnorm
+    rng = np.random.default_rng(0)
+    h = rng.standard_normal((37, 256)).astype(np.float32) * 3
+    ht = torch.from_numpy(h).cuda()
+    x = torch.empty((37, 256), dtype=torch.bfloat16, device="cuda")
+    rmsnorm(ht, x, 1e-6)
+    ref = orc.rms_norm(h, 1e-6)
+    assert _rel(_host(x), ref) < 4e-3
+    o = torch.from_numpy(rng.standard_normal((37, 256)).astype(np.float32)).cuda()
+    residual_add(ht, o)
+    assert np.allclose(_host(ht), np.float64(h) + _host(o), rtol=1e-6, atol=1e-6)
