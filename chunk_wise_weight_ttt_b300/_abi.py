@@ -15,6 +15,7 @@ TTT_OK, TTT_EINVAL, TTT_EUNSUPPORTED, TTT_ECUDA, TTT_ETIMEOUT, TTT_EFAULT_INJECT
 STATUS_NAMES = {0: "TTT_OK", 1: "TTT_EINVAL", 2: "TTT_EUNSUPPORTED", 3: "TTT_ECUDA",
                 4: "TTT_ETIMEOUT", 5: "TTT_EFAULT_INJECTED"}
 TTT_F32, TTT_BF16 = 0, 1
+NOALLOC_SCRATCH_BYTES = 32 << 20  # TTT_NOALLOC_SCRATCH_BYTES in the header
 
 
 class Config(C.Structure):
@@ -46,6 +47,8 @@ SIGNATURES = {
     "ttt_mlp_profile_enable": (_st, [_vp, _i32]),
     "ttt_mlp_profile_read": (_st, [_vp, C.POINTER(C.c_float), C.POINTER(_i64)]),
     "ttt_mlp_intermediates": (_st, [_vp, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_i32)]),
+    "ttt_target_noalloc": (_st, [_vp, _vp, _vp, _i64, _i32, _i32, _i32, C.POINTER(_i64), _i32,
+                                 C.c_float, _vp, _vp, _vp]),
     "ttt_rmsnorm": (_st, [_vp, _vp, _i64, _i32, C.c_float, _i32, _vp]),
     "ttt_residual_add": (_st, [_vp, _vp, _i64, _i32, _i32, _vp]),
 }

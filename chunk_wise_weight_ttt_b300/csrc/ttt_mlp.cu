@@ -12,6 +12,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -789,3 +790,127 @@ ttt_status ttt_residual_add(float* hs, const void* o, int64_t n, int32_t d, int3
 }
 
 }  // extern "C"
+
+// ====================================================================== allocation-free target
+
+// Scratch of ttt_target_noalloc: one file-scope device array per GPU that
+// loads the library.  Host code only ever sees a host-side stand-in for this
+// name, so the device address is looked up once per device and passed in.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TTT_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_ptr[kNoallocMaxDevices] = {};
+int g_noalloc_sms[kNoallocMaxDevices] = {};
+
+// One-time set-up of the current device: scratch address and kernel attributes.
+ttt_status noalloc_setup(int dev, unsigned char** ptr, int* sms) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess)
+      return fail(nullptr, TTT_ECUDA, std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e));
+    e = cudaFuncSetAttribute((const void*)tc_gemm_kernel<kVProj>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+    if (e != cudaSuccess)
+      return fail(nullptr, TTT_ECUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+      return fail(nullptr, TTT_ECUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+    g_noalloc_sms[dev] = n;
+    g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
+  }
+  *ptr = g_noalloc_ptr[dev];
+  *sms = g_noalloc_sms[dev];
+  return TTT_OK;
+}
+
+}  // namespace
+
+extern "C" ttt_status ttt_target_noalloc(const void* x0, const void* conv_w, const void* w_target,
+                                         int64_t n_tokens, int32_t d, int32_t conv_k, int32_t chunk,
+                                         const int64_t* doc_starts, int32_t n_doc_starts, float eta,
+                                         void* v, int32_t* status, void* stream) {
+  if (d < 256 || d % 64) return fail(nullptr, TTT_EINVAL, "ttt_target_noalloc: d must be a multiple of 64, >= 256");
+  if (chunk < 1 || chunk > 1024) return fail(nullptr, TTT_EINVAL, "ttt_target_noalloc: chunk must be in 1..1024");
+  if (conv_k < 1 || conv_k > 8) return fail(nullptr, TTT_EINVAL, "ttt_target_noalloc: conv_k must be in 1..8");
+  if (n_tokens < 0 || !std::isfinite(eta)) return fail(nullptr, TTT_EINVAL, "ttt_target_noalloc: bad n_tokens or eta");
+  if (n_doc_starts < 0 || (n_doc_starts > 0 && !doc_starts))
+    return fail(nullptr, TTT_EINVAL, "ttt_target_noalloc: doc_starts is NULL but n_doc_starts > 0");
+  for (int i = 0; i < n_doc_starts; ++i) {
+    if (doc_starts[i] < 0 || doc_starts[i] >= n_tokens || (i > 0 && doc_starts[i] <= doc_starts[i - 1]))
+      return fail(nullptr, TTT_EINVAL, "ttt_target_noalloc: document starts must be strictly increasing in [0, n_tokens)");
+  }
+  const uint64_t need = 2ull * d * d + 2ull * (uint64_t)n_tokens * d + 512;
+  if (need > TTT_NOALLOC_SCRATCH_BYTES) {
+    char buf[200];
+    std::snprintf(buf, sizeof buf,
+                  "ttt_target_noalloc: needs %llu scratch bytes (2*d*d + 2*n_tokens*d + 512), more than the "
+                  "fixed %u-byte array", (unsigned long long)need, (unsigned)TTT_NOALLOC_SCRATCH_BYTES);
+    return fail(nullptr, TTT_EUNSUPPORTED, buf);
+  }
+  if (n_tokens == 0) return TTT_OK;
+  if (!x0 || !conv_w || !w_target || !v) return fail(nullptr, TTT_EINVAL, "ttt_target_noalloc: NULL buffer");
+  if (!aligned16(x0) || !aligned16(conv_w) || !aligned16(w_target) || !aligned16(v))
+    return fail(nullptr, TTT_EINVAL, "ttt_target_noalloc: buffers must be 16-byte aligned");
+
+  int dev = 0;
+  TTT_CK(nullptr, cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoallocMaxDevices) return fail(nullptr, TTT_EUNSUPPORTED, "ttt_target_noalloc: device ordinal too large");
+  unsigned char* scratch = nullptr;
+  int sms = 0;
+  ttt_status s = noalloc_setup(dev, &scratch, &sms);
+  if (s != TTT_OK) return s;
+
+  // scratch layout: [0,256) control (tile counter, error word) | W_target^T | U
+  int* ctrl = reinterpret_cast<int*>(scratch);
+  __nv_bfloat16* wtT = reinterpret_cast<__nv_bfloat16*>(scratch + 256);
+  __nv_bfloat16* u = reinterpret_cast<__nv_bfloat16*>(scratch + 256 + align_up(2ull * d * d, 256));
+  int* err = status ? status : ctrl + 1;
+  cudaStream_t st = (cudaStream_t)stream;
+
+  TTT_CK(nullptr, cudaMemsetAsync(ctrl, 0, 256, st));
+  if (status) TTT_CK(nullptr, cudaMemsetAsync(status, 0, sizeof(int32_t), st));
+  dim3 tb(32, 8), tg((d + 31) / 32, (d + 31) / 32);
+  transpose_kernel<__nv_bfloat16><<<tg, tb, 0, st>>>((const __nv_bfloat16*)w_target, wtT, d, d);
+  TTT_CK(nullptr, cudaGetLastError());
+
+  std::vector<Span> docs = plan_groups(n_tokens, chunk, 1 << 30, doc_starts, n_doc_starts);
+  for (size_t w0 = 0; w0 < docs.size(); w0 += kMaxSpans) {
+    const size_t w1 = std::min(docs.size(), w0 + kMaxSpans);
+    SpanList sl{};
+    sl.n = (int)(w1 - w0);
+    sl.chunk = chunk;
+    for (size_t i = w0; i < w1; ++i) {
+      sl.start[i - w0] = docs[i].start;
+      sl.len[i - w0] = docs[i].len;
+    }
+    const long long cnt = (long long)(docs[w1 - 1].start + docs[w1 - 1].len - docs[w0].start) * (d / 8);
+    conv_target_kernel<__nv_bfloat16, __nv_bfloat16><<<grid_for(cnt, 256), 256, 0, st>>>(
+        (const __nv_bfloat16*)x0, (const __nv_bfloat16*)conv_w, u, d, conv_k, sl);
+    TTT_CK(nullptr, cudaGetLastError());
+  }
+
+  std::string why;
+  GemmArgs a;
+  std::memset(&a, 0, sizeof a);
+  if (!make_map(&a.map[0], u, d, n_tokens, d, 64, 128, &why) ||
+      !make_map(&a.map[1], wtT, d, d, d, 64, 256, &why))
+    return fail(nullptr, TTT_ECUDA, why);
+  a.n_rows = (int)n_tokens;
+  a.d = d;
+  a.f = d;
+  a.chunk = chunk;
+  a.alpha = eta;
+  a.counter = ctrl;
+  a.err = err;
+  a.out0 = v;
+  const int ntiles = ((int)n_tokens + kBM - 1) / kBM * ((d + kBN - 1) / kBN);
+  tc_gemm_kernel<kVProj><<<std::max(1, std::min(sms, ntiles)), kGemmThreads, kGemmSmemBytes, st>>>(a);
+  TTT_CK(nullptr, cudaGetLastError());
+  return TTT_OK;
+}

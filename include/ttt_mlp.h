@@ -157,6 +157,43 @@ ttt_status ttt_mlp_profile_read(ttt_mlp* h, float* ms, int64_t* counts);
  * tensor-core path) or "simt" (fp32 FFMA path).  Host only. */
 const char* ttt_mlp_path(const ttt_mlp* h);
 
+/* ---- allocation-free target computation ----
+ *
+ * The paper has no counterpart to this call; it exists for callers that may
+ * not allocate device memory at all (for example code that runs inside
+ * another runtime's memory pool or an allocator-free embedded host, where
+ * cudaMalloc is forbidden or unavailable) and so cannot provide the
+ * workspace the handle-based calls need.
+ *
+ * It computes the same target as a forward call, V = eta * Conv1D(X0) W_target
+ * (chunk-local, causal-shifted depthwise Conv1D; chunking restarts at each
+ * document start), into the caller's v, with the bf16 tensor-core kernels.
+ * Its scratch (the Conv1D output, the transposed W_target, a tile counter and
+ * an error word) lives in one file-scope device array of
+ * TTT_NOALLOC_SCRATCH_BYTES bytes that every GPU which loads the library
+ * holds until the process exits; the call allocates nothing.
+ *
+ * x0: n_tokens x d bf16; conv_w: conv_k x d bf16; w_target: d x d bf16
+ * (in x out); v: n_tokens x d bf16 output; all device, 16-byte aligned.
+ * d must be a multiple of 64 and >= 256; 1 <= chunk <= 1024; 1 <= conv_k <= 8;
+ * doc_starts as in ttt_mlp_forward_chunks.  A call whose scratch need,
+ * 2*d*d + 2*n_tokens*d bytes plus 512, exceeds TTT_NOALLOC_SCRATCH_BYTES
+ * returns TTT_EUNSUPPORTED before anything is enqueued.
+ *
+ * The first call on a device sets up that device (it looks up the scratch
+ * array's device address and configures the kernel); make that first call
+ * before any CUDA stream capture.  Every call on a device shares the one
+ * array and the call clears what must start at zero, so calls whose kernels
+ * overlap on the GPU (different streams, or different host threads) race and
+ * must be serialised by the caller.  status: optional device int32 that
+ * receives 0, or the code of an in-kernel wait that ran out (the output is
+ * then incomplete); may be NULL. */
+#define TTT_NOALLOC_SCRATCH_BYTES (32u << 20)
+ttt_status ttt_target_noalloc(const void* x0, const void* conv_w, const void* w_target,
+                              int64_t n_tokens, int32_t d, int32_t conv_k, int32_t chunk,
+                              const int64_t* doc_starts, int32_t n_doc_starts, float eta,
+                              void* v, int32_t* status, void* stream);
+
 /* ---- residual-stack glue (pre-norm blocks h <- h + MLP_TTT(RMSNorm(h))) ---- */
 
 /* x[t] = RMSNorm(h[t]) = h[t] / sqrt(mean(h[t]^2) + eps), unit gain, cast to
