@@ -140,6 +140,16 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// Copy a 128-row x 256-bit block (8 fp32 columns per row) from shared memory
+// into TMEM: smem row r -> TMEM lane r, columns [taddr.col, taddr.col + 8).
+// The source is described by a shared-memory matrix descriptor exactly like an
+// MMA operand (here K-major with 128-byte swizzle), and the copy is ordered with
+// the tcgen05.mma ops issued before and after it by the same thread.  One
+// thread issues.
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(

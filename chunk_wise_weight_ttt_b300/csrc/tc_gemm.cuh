@@ -21,10 +21,15 @@
 //              O_g = Z_g W_s^T + S_g V_g            (W_s = state at group start)
 //            and the update tiles
 //              W <- W_s + V_g^T Z_g,  Wb_next <- bf16(W)
-//            in one launch.  Applying W_s to every chunk of the group plus the
-//            intra-group correction S_g V_g equals applying each chunk's own
-//            pre-update state (the deltas are additive, appendix B of the
-//            "In-Place Test-Time Training" summary page).
+//            in one launch.  An update tile first streams its fp32 block of
+//            W_s through the operand ring into the TMEM accumulator
+//            (tcgen05.cp), so the MMAs accumulate straight onto the fast
+//            weight and the epilogue only stores (W and its bf16 copy),
+//            coalesced through a per-warp shared-memory transpose.
+//            Applying W_s to every chunk of the group plus the intra-group
+//            correction S_g V_g equals applying each chunk's own pre-update
+//            state (the deltas are additive, appendix B of the "In-Place
+//            Test-Time Training" summary page).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -47,6 +52,16 @@ constexpr int kSchedRing = 4;
 constexpr int kGemmThreads = 192;
 constexpr int kMaxGroups = 256;
 constexpr int kSwizzleGroupM = 16;
+// fp32 fast-weight preload of an update tile: boxes of 32 columns x 128 rows
+// (128-byte rows, 16 KB), three per ring stage.
+constexpr int kWBoxCols = 32;
+constexpr int kWBoxBytes = kBM * kWBoxCols * 4;
+constexpr int kWBoxesPerStage = kStageBytes / kWBoxBytes;
+constexpr int kWBoxes = kBN / kWBoxCols;
+constexpr int kWPreBlocks = (kWBoxes + kWBoxesPerStage - 1) / kWBoxesPerStage;
+// per-warp staging for the transposed (coalesced) update-tile stores
+constexpr int kStgBytesPerWarp = 32 * 128;
+constexpr int kEpiWarps = 4;
 
 enum GemmMode : int { kSwiGLU = 0, kVProj = 1, kSGram = 2, kGroup = 3 };
 
@@ -56,9 +71,10 @@ enum GemmMode : int { kSwiGLU = 0, kVProj = 1, kSGram = 2, kGroup = 3 };
 //   kSGram:  0 Z (64x128), 1 Z (64x256)
 //   kGroup:  0 Z (64x128), 1 W_s bf16 (64x256), 2 S (64x128),
 //            3 V MN-major (64x64), 4 V MN-major with the group's K extent,
-//            5 Z MN-major (64x64) with the group's K extent
+//            5 Z MN-major (64x64) with the group's K extent,
+//            6 W fp32 of the slot (32 columns x 128 rows)
 struct GemmArgs {
-  CUtensorMap map[6];
+  CUtensorMap map[7];
   int n_rows;    // tokens of the call (rows of X/Z/U/V/O)
   int d, f;
   int chunk;
@@ -68,20 +84,20 @@ struct GemmArgs {
   void* out0;    // kSwiGLU: Z; kVProj: V; kSGram: S; kGroup: O
   void* out1;    // kGroup: W (fp32, updated in place)
   void* out2;    // kGroup: Wb_next (bf16)
-  const void* in0;  // kGroup: W_0 (bf16) when the group starts a document
   // groups
   int s_pad;         // row/column pitch of one S block (multiple of 256)
   int n_groups;      // kSGram
   int g_start[kMaxGroups];
   int g_len[kMaxGroups];
-  int g0, glen, gslot, reset;  // kGroup
+  int g0, glen, gslot;  // kGroup
 };
 
 struct TileInfo {
   int kind;  // 0 plain/apply, 1 update
   int m0, n0;
   int g;
-  int nkb1, nkb2;
+  int npre;        // leading ring blocks that preload the accumulator (update tiles)
+  int nkb1, nkb2;  // MMA K blocks: main operands, then the intra-group correction
   bool valid;
 };
 
@@ -109,6 +125,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t) {
   TileInfo ti{};
   ti.valid = true;
   ti.nkb2 = 0;
+  ti.npre = 0;
   ti.kind = 0;
   ti.g = 0;
   if (MODE == kSwiGLU) {
@@ -149,16 +166,36 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t) {
       ti.kind = 1;
       ti.m0 = (u / ntU) * kBM;
       ti.n0 = (u % ntU) * kBN;
+      ti.npre = kWPreBlocks;
       ti.nkb1 = cdiv(a.glen, kBK);
     }
   }
   return ti;
 }
 
-// Issue the TMA loads of K block `kb` of tile `ti` into stage buffers sa / sb.
+// Bytes that ring block `kb` of tile `ti` brings in.
+template <int MODE>
+__device__ __forceinline__ uint32_t kblock_bytes(const TileInfo& ti, int kb) {
+  if (MODE == kGroup && kb < ti.npre)
+    return static_cast<uint32_t>(min(kWBoxesPerStage, kWBoxes - kb * kWBoxesPerStage)) * kWBoxBytes;
+  return kStageBytes;
+}
+
+// Issue the TMA loads of ring block `kb` of tile `ti` into stage buffers sa / sb
+// (for an update tile the first npre blocks are its fp32 W boxes, then the K
+// blocks of the MMA operands).
 template <int MODE>
 __device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& ti, int kb,
-                                            uint8_t* sa, uint8_t* sb, uint64_t* bar) {
+                                             uint8_t* sa, uint8_t* sb, uint64_t* bar) {
+  if (MODE == kGroup && ti.kind == 1) {
+    if (kb < ti.npre) {
+      const int b0 = kb * kWBoxesPerStage, b1 = min(b0 + kWBoxesPerStage, kWBoxes);
+      for (int b = b0; b < b1; ++b)
+        tma_load_2d(sa + (b - b0) * kWBoxBytes, &a.map[6], bar, ti.n0 + b * kWBoxCols, ti.m0);
+      return;
+    }
+    kb -= ti.npre;
+  }
   if (MODE == kSwiGLU) {
     tma_load_2d(sa, &a.map[0], bar, kb * kBK, ti.m0);
     tma_load_2d(sb, &a.map[1], bar, kb * kBK, ti.n0);
@@ -183,7 +220,7 @@ __device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& t
           tma_load_2d(sb + q * 8192, &a.map[3], bar, ti.n0 + q * 64, a.g0 + k2);
       }
     } else {
-      const int k = a.g0 + kb * kBK;
+      const int k = a.g0 + kb * kBK;  // kb already excludes the preload blocks
 #pragma unroll
       for (int q = 0; q < kBM / 64; ++q)
         tma_load_2d(sa + q * 8192, &a.map[4], bar, ti.m0 + q * 64, k);
@@ -209,6 +246,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
+                                             uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
+               "r"(w)
+               : "memory");
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t (&v)[4]) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(addr)
+               : "memory");
+}
+
 // Store 32 consecutive bf16 values (packed in 16 words) if the 8-groups are in range.
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t (&p)[16],
                                               int cols_left) {
@@ -223,7 +274,7 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t
 
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo& ti,
-                                              uint32_t tacc, int row) {
+                                              uint32_t tacc, int row, uint8_t* stg) {
   uint32_t r[32];
   if (MODE == kSwiGLU) {
     const int grow = ti.m0 + row;
@@ -247,58 +298,40 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
     }
   } else if (MODE == kVProj || MODE == kGroup) {
     if (MODE == kGroup && ti.kind == 1) {
-      // fast-weight update: W <- base + acc; Wb_next <- bf16(W)
-      const int wr = ti.m0 + row;
-      float* wrow = reinterpret_cast<float*>(a.out1) + (size_t)wr * a.f;
-      __nv_bfloat16* brow = reinterpret_cast<__nv_bfloat16*>(a.out2) + (size_t)wr * a.f;
-      const __nv_bfloat16* w0row =
-          reinterpret_cast<const __nv_bfloat16*>(a.in0) + (size_t)wr * a.f;
+      // fast-weight update: the accumulator already holds W_s + V^T Z.  Each
+      // 32-column slice of the warp's 32 rows goes registers -> staging
+      // (row per thread, 16-byte chunks XOR-swizzled by row so both phases are
+      // bank-conflict free) -> 4 full rows per store instruction.
+      const int lane = row & 31;
+      const int rbase = ti.m0 + (row - lane);
+      float* W = reinterpret_cast<float*>(a.out1);
+      __nv_bfloat16* Wb = reinterpret_cast<__nv_bfloat16*>(a.out2);
+      const uint32_t st_row = smem_u32(stg) + lane * 128;
 #pragma unroll 1
       for (int s = 0; s < kBN / 32; ++s) {
-        const int col = ti.n0 + s * 32;
         tmem_ld32(tacc + s * 32, r);
         tmem_ld_wait(r);
-        if (wr >= a.d) continue;
-        float base[32];
-        if (a.reset) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (col + q * 8 < a.f) {
-              uint4 v = *reinterpret_cast<const uint4*>(w0row + col + q * 8);
-              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+        for (int q = 0; q < 8; ++q)
+          st_shared_v4(st_row + ((q ^ (lane & 7)) << 4), r[4 * q], r[4 * q + 1], r[4 * q + 2],
+                       r[4 * q + 3]);
+        __syncwarp();
+        const int cq = lane & 7;
+        const int col = ti.n0 + s * 32 + cq * 4;
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float2 ff = __bfloat1622float2(h[e]);
-                base[q * 8 + 2 * e] = ff.x;
-                base[q * 8 + 2 * e + 1] = ff.y;
-              }
-            }
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            if (col + q * 4 < a.f) {
-              float4 v = *reinterpret_cast<const float4*>(wrow + col + q * 4);
-              base[4 * q] = v.x;
-              base[4 * q + 1] = v.y;
-              base[4 * q + 2] = v.z;
-              base[4 * q + 3] = v.w;
-            }
+        for (int j = 0; j < 8; ++j) {
+          const int rr = j * 4 + (lane >> 3);
+          uint32_t v[4];
+          ld_shared_v4(smem_u32(stg) + rr * 128 + ((cq ^ (rr & 7)) << 4), v);
+          const int wr = rbase + rr;
+          if (wr < a.d && col < a.f) {
+            *reinterpret_cast<uint4*>(W + (size_t)wr * a.f + col) = make_uint4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<uint2*>(Wb + (size_t)wr * a.f + col) =
+                make_uint2(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                           pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])));
           }
         }
-        float w[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) w[j] = base[j] + __uint_as_float(r[j]);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (col + q * 4 < a.f)
-            *reinterpret_cast<float4*>(wrow + col + q * 4) =
-                make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-        }
-        uint32_t p[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) p[j] = pack_bf16x2(w[2 * j], w[2 * j + 1]);
-        store_bf16x32(brow + col, p, a.f - col);
+        __syncwarp();
       }
     } else {
       // plain bf16 store of alpha * acc (kVProj) or acc (kGroup apply)
@@ -361,6 +394,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   int* sched_item = reinterpret_cast<int*>(drain + 1);  // [kSchedRing]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sched_item + kSchedRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* staging = smem + kStages * kStageBytes + 1024;  // [kEpiWarps][kStgBytesPerWarp]
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -396,7 +430,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     if (lane == 0) {
       // ---------------- TMA producer + tile scheduler
 #pragma unroll 1
-      for (int q = 0; q < 6; ++q) tma_prefetch_desc(&a.map[q]);
+      for (int q = 0; q < 7; ++q) tma_prefetch_desc(&a.map[q]);
       int stage = 0;
       uint32_t phase = 0;
       int fills = 0;
@@ -412,7 +446,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         if (t >= ntiles) break;
         const TileInfo ti = decode_tile<MODE>(a, t);
         if (!ti.valid) continue;
-        const int nkb = ti.nkb1 + ti.nkb2;
+        const int nkb = ti.npre + ti.nkb1 + ti.nkb2;
 #pragma unroll 1
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.err, kErrWaitSmemEmpty)) {
@@ -420,7 +454,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             break;
           }
           uint8_t* sa = stage_base + stage * kStageBytes;
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          mbar_arrive_expect_tx(&full[stage], kblock_bytes<MODE>(ti, kb));
           load_kblock<MODE>(a, ti, kb, sa, sa + kABytes, &full[stage]);
           ++fills;
           if (++stage == kStages) {
@@ -462,7 +496,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           break;
         tc_fence_after();
         const uint32_t tacc = tmem_base + buf * kBN;
-        const int nkb = ti.nkb1 + ti.nkb2;
+        const int nkb = ti.npre + ti.nkb1 + ti.nkb2;
 #pragma unroll 1
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, a.err, kErrWaitTmaFull)) {
@@ -471,16 +505,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(stage_base + stage * kStageBytes);
-          const uint32_t sb = sa + kABytes;
-          const int lay = kblock_layout<MODE>(ti, kb);
-          const uint32_t idesc = idesc_bf16_f32(kBM, kBN, lay == 2, lay >= 1);
+          if (kb < ti.npre) {
+            // fp32 W boxes (128 rows x 128 B, 128-byte swizzle) -> accumulator
+            // columns, 8 columns per copy
+            const int b0 = kb * kWBoxesPerStage, b1 = min(b0 + kWBoxesPerStage, kWBoxes);
+            for (int b = b0; b < b1; ++b) {
+              const uint32_t src = sa + (b - b0) * kWBoxBytes;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = (lay == 2) ? sdesc_sw128(sa + k * 2048, 8192, 1024)
-                                           : sdesc_sw128(sa + k * 32, 0, 1024);
-            const uint64_t bd = (lay >= 1) ? sdesc_sw128(sb + k * 2048, 8192, 1024)
-                                           : sdesc_sw128(sb + k * 32, 0, 1024);
-            tc_mma_bf16(tacc, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+              for (int j = 0; j < kWBoxCols / 8; ++j)
+                tc_cp_128x256b(tacc + b * kWBoxCols + j * 8, sdesc_sw128(src + j * 32, 0, 1024));
+            }
+          } else {
+            const int kk = kb - ti.npre;
+            const uint32_t sb = sa + kABytes;
+            const int lay = kblock_layout<MODE>(ti, kk);
+            const uint32_t idesc = idesc_bf16_f32(kBM, kBN, lay == 2, lay >= 1);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint64_t ad = (lay == 2) ? sdesc_sw128(sa + k * 2048, 8192, 1024)
+                                             : sdesc_sw128(sa + k * 32, 0, 1024);
+              const uint64_t bd = (lay >= 1) ? sdesc_sw128(sb + k * 2048, 8192, 1024)
+                                             : sdesc_sw128(sb + k * 32, 0, 1024);
+              tc_mma_bf16(tacc, ad, bd, idesc, (ti.npre > 0 || kk > 0 || k > 0) ? 1u : 0u);
+            }
           }
           tc_commit(&empty[stage]);
           if (++stage == kStages) {
@@ -526,7 +573,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       if (!ok) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + buf * kBN;
-      epilogue_tile<MODE>(a, ti, tacc, row);
+      epilogue_tile<MODE>(a, ti, tacc, row, staging + (warp - 2) * kStgBytesPerWarp);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
@@ -542,6 +589,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   }
 }
 
-constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kGemmSmemBytes =
+    1024 /*align*/ + kStages * kStageBytes + 1024 /*barriers*/ + kEpiWarps * kStgBytesPerWarp;
+static_assert(kGemmSmemBytes <= 232448, "exceeds the opt-in shared memory of one CTA");
 
 }  // namespace ttt

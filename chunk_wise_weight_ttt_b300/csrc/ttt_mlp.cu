@@ -144,20 +144,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 matrix [outer x inner] row-major with row pitch `pitch` elements; box
-// (box_inner x box_outer) with 128-byte swizzle, zero fill outside.
+// Matrix [outer x inner] row-major with row pitch `pitch` elements (bf16, or
+// fp32 when `f32`); box (box_inner x box_outer) with 128-byte swizzle, zero
+// fill outside.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
-              uint32_t box_inner, uint32_t box_outer, std::string* why) {
+              uint32_t box_inner, uint32_t box_outer, std::string* why, bool f32 = false) {
   auto fn = encode_fn();
   if (!fn) {
     *why = "cuTensorMapEncodeTiled is unavailable";
     return false;
   }
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {pitch * 2};
+  cuuint64_t strides[1] = {pitch * (f32 ? 4 : 2)};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -334,6 +336,8 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
 
   const size_t wsz = (size_t)d * f;
   float* W = h->W + (size_t)doc * wsz;
+  CUtensorMap map_wf;  // the slot's fp32 fast weight, update-tile preload boxes
+  if (!make_map(&map_wf, W, f, d, f, 32, 128, &why, /*f32=*/true)) return fail(h, TTT_ECUDA, why);
   for (size_t w0 = 0; w0 < groups.size(); w0 += (size_t)h->s_slots) {
     const size_t w1 = std::min(groups.size(), w0 + (size_t)h->s_slots);
     // intra-group Gram blocks S_g = mask(Z_g Z_g^T) of this wave
@@ -365,7 +369,14 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
 
     for (size_t i = w0; i < w1; ++i) {
       const Span& g = groups[i];
-      if (!g.reset && h->wb_owner != doc) {
+      if (g.reset) {
+        // document start: W <- W_0 (the update tiles accumulate onto W; the
+        // apply tiles read W_0's bf16 values directly)
+        to_f32_kernel<__nv_bfloat16><<<grid_for((long long)wsz, 256), 256, 0, st>>>(
+            (const __nv_bfloat16*)h->w0, W, (long long)wsz);
+        TTT_CK_LAUNCH(h);
+        h->prof_launches++;
+      } else if (h->wb_owner != doc) {
         to_bf16_kernel<<<grid_for((long long)wsz, 256), 256, 0, st>>>(W, h->Wb[h->wb_cur], (long long)wsz);
         TTT_CK_LAUNCH(h);
         h->prof_launches++;
@@ -376,6 +387,7 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
       q.map[1] = g.reset ? h->map_w0 : h->map_wb[h->wb_cur];
       q.map[2] = h->map_s;
       q.map[3] = map_vmn;
+      q.map[6] = map_wf;
       const bool exact = (g.len % kBK == 0) || ((int64_t)g.start + g.len == n);
       if (exact) {
         q.map[4] = map_vmn;
@@ -389,11 +401,9 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
       q.out0 = o;
       q.out1 = W;
       q.out2 = h->Wb[h->wb_cur ^ 1];
-      q.in0 = h->w0;
       q.g0 = g.start;
       q.glen = g.len;
       q.gslot = (int)(i - w0);
-      q.reset = g.reset ? 1 : 0;
       q.counter = next_counter(h, st);
       const int nt = ((g.len + kBM - 1) / kBM) * ((d + kBN - 1) / kBN) +
                      ((d + kBM - 1) / kBM) * ((f + kBN - 1) / kBN);

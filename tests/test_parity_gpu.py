@@ -76,11 +76,13 @@ def _check_layer(cfg, tol, ttt_tol=None, force_simt=False, expect_path=None):
     if ttt_tol is not None:
         o_static, _ = _oracle(cfg, eta=0.0)
         part_gpu, part_ref = _host(o) - o_static, o_ref - o_static
-        ep = _rel(part_gpu, part_ref)
         frac = np.linalg.norm(part_ref) / np.linalg.norm(o_ref)
-        msg += f"  TTT-part err {ep:.3e} (TTT part is {frac:.1%} of O)"
         if frac > 1e-6:  # a single chunk has no TTT part
+            ep = _rel(part_gpu, part_ref)
+            msg += f"  TTT-part err {ep:.3e} (TTT part is {frac:.1%} of O)"
             assert ep <= ttt_tol, msg
+        else:
+            msg += "  (no TTT part: one chunk)"
     print(msg)
     assert eo <= tol and ew <= tol, msg
     return layer
