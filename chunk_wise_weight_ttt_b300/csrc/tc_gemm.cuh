@@ -1,9 +1,17 @@
 // Persistent, warp-specialised tcgen05 GEMM engine for the bf16 hot path.
 //
-// One CTA per SM, 192 threads:
-//   warp 0      TMA producer: takes tiles from a dynamic tile counter, streams
-//               the A/B operand blocks (64 K-elements each) into a 4-stage
-//               shared-memory ring with 128-byte swizzle.
+// CTAs run in clusters of two (one CTA per SM).  The pair works on two
+// vertically adjacent 128x256 tiles that share their B operand: each CTA loads
+// its own A block and one half of the common B block, which TMA multicasts into
+// both CTAs' shared memory, so a CTA reads 32 of the 48 KB of every ring stage
+// from L2.  The leader CTA (rank 0) claims tile pairs from a dynamic counter
+// and hands each to its peer through distributed shared memory; a ring stage is
+// refilled only after both CTAs' MMAs have released it.
+//
+// Each CTA has 192 threads:
+//   warp 0      TMA producer: streams the operand blocks (64 K-elements each)
+//               of the CTA's tile into a 4-stage shared-memory ring with
+//               128-byte swizzle.
 //   warp 1      owns the TMEM allocation (512 columns = two 128x256 fp32
 //               accumulators) and issues tcgen05.mma from one thread.
 //   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (one TMEM
@@ -51,7 +59,8 @@ constexpr int kTmemCols = 2 * kBN;              // two fp32 accumulators
 constexpr int kSchedRing = 4;
 constexpr int kGemmThreads = 192;
 constexpr int kMaxGroups = 256;
-constexpr int kSwizzleGroupM = 16;
+constexpr int kSwizzlePairs = 8;   // SwiGLU raster: tile pairs per column sweep
+constexpr uint16_t kPairMask = 0x3;  // both CTAs of the cluster
 // fp32 fast-weight preload of an update tile: boxes of 32 columns x 128 rows
 // (128-byte rows, 16 KB), three per ring stage.
 constexpr int kWBoxCols = 32;
@@ -65,11 +74,11 @@ constexpr int kEpiWarps = 4;
 
 enum GemmMode : int { kSwiGLU = 0, kVProj = 1, kSGram = 2, kGroup = 3 };
 
-// Tensor-map slots per mode.
+// Tensor-map slots per mode (B boxes are the half that one CTA of a pair loads).
 //   kSwiGLU: 0 X (box 64x128), 1 Wg (64x128), 2 Wu (64x128)
-//   kVProj:  0 U (64x128), 1 W_target^T (64x256)
-//   kSGram:  0 Z (64x128), 1 Z (64x256)
-//   kGroup:  0 Z (64x128), 1 W_s bf16 (64x256), 2 S (64x128),
+//   kVProj:  0 U (64x128), 1 W_target^T (64x128)
+//   kSGram:  0 Z (64x128), 1 Z (64x128)
+//   kGroup:  0 Z (64x128), 1 W_s bf16 (64x128), 2 S (64x128),
 //            3 V MN-major (64x64), 4 V MN-major with the group's K extent,
 //            5 Z MN-major (64x64) with the group's K extent,
 //            6 W fp32 of the slot (32 columns x 128 rows)
@@ -79,7 +88,7 @@ struct GemmArgs {
   int d, f;
   int chunk;
   float alpha;   // eta for kVProj
-  int* counter;  // dynamic tile counter, zero at launch
+  int* counter;  // dynamic tile-pair counter, zero at launch
   int* err;      // workspace error word
   void* out0;    // kSwiGLU: Z; kVProj: V; kSGram: S; kGroup: O
   void* out1;    // kGroup: W (fp32, updated in place)
@@ -112,16 +121,21 @@ __device__ __forceinline__ int corr_kbound(int len, int m, int chunk) {
   return cdiv(cs, kBK) * kBK;
 }
 
+// Number of tile pairs (work items of a cluster).  Pair p covers the 128-row
+// blocks 2*mp and 2*mp + 1 (one per CTA) of one column block.
 template <int MODE>
 __device__ __forceinline__ int num_tiles(const GemmArgs& a) {
-  if (MODE == kSwiGLU) return cdiv(a.n_rows, kBM) * cdiv(a.f, kBM);
-  if (MODE == kVProj) return cdiv(a.n_rows, kBM) * cdiv(a.d, kBN);
-  if (MODE == kSGram) return a.n_groups * cdiv(a.s_pad, kBM) * cdiv(a.s_pad, kBN);
-  return cdiv(a.glen, kBM) * cdiv(a.d, kBN) + cdiv(a.d, kBM) * cdiv(a.f, kBN);
+  if (MODE == kSwiGLU) return cdiv(cdiv(a.n_rows, kBM), 2) * cdiv(a.f, kBM);
+  if (MODE == kVProj) return cdiv(cdiv(a.n_rows, kBM), 2) * cdiv(a.d, kBN);
+  if (MODE == kSGram) return a.n_groups * cdiv(cdiv(a.s_pad, kBM), 2) * cdiv(a.s_pad, kBN);
+  return cdiv(cdiv(a.glen, kBM), 2) * cdiv(a.d, kBN) + cdiv(cdiv(a.d, kBM), 2) * cdiv(a.f, kBN);
 }
 
+// The tile of pair `t` that CTA `rank` computes.  Everything that decides the
+// ring's block sequence (validity, block counts) depends on the pair only, so
+// both CTAs stream identical B blocks in the same order.
 template <int MODE>
-__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t) {
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int rank) {
   TileInfo ti{};
   ti.valid = true;
   ti.nkb2 = 0;
@@ -129,42 +143,46 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t) {
   ti.kind = 0;
   ti.g = 0;
   if (MODE == kSwiGLU) {
-    const int mt = cdiv(a.n_rows, kBM), nt = cdiv(a.f, kBM);
-    const int gsz = kSwizzleGroupM * nt;
-    const int gid = t / gsz, first = gid * kSwizzleGroupM;
-    const int gm = min(kSwizzleGroupM, mt - first);
+    const int mpt = cdiv(cdiv(a.n_rows, kBM), 2), nt = cdiv(a.f, kBM);
+    const int gsz = kSwizzlePairs * nt;
+    const int gid = t / gsz, first = gid * kSwizzlePairs;
+    const int gm = min(kSwizzlePairs, mpt - first);
     const int w = t % gsz;
-    ti.m0 = (first + w % gm) * kBM;
+    ti.m0 = (2 * (first + w % gm) + rank) * kBM;
     ti.n0 = (w / gm) * kBM;
     ti.nkb1 = cdiv(a.d, kBK);
   } else if (MODE == kVProj) {
     const int nt = cdiv(a.d, kBN);
-    ti.m0 = (t / nt) * kBM;
+    ti.m0 = (2 * (t / nt) + rank) * kBM;
     ti.n0 = (t % nt) * kBN;
     ti.nkb1 = cdiv(a.d, kBK);
   } else if (MODE == kSGram) {
-    const int mt = cdiv(a.s_pad, kBM), nt = cdiv(a.s_pad, kBN);
-    const int g = t / (mt * nt), r = t % (mt * nt);
-    const int m = r / nt, n = r % nt;
+    const int mpt = cdiv(cdiv(a.s_pad, kBM), 2), nt = cdiv(a.s_pad, kBN);
+    const int g = t / (mpt * nt), r = t % (mpt * nt);
+    const int mp = r / nt, n = r % nt;
     const int len = a.g_len[g];
     ti.g = g;
-    ti.m0 = m * kBM;
+    ti.m0 = (2 * mp + rank) * kBM;
     ti.n0 = n * kBN;
-    ti.valid = (ti.m0 < len) && (ti.n0 < corr_kbound(len, m, a.chunk));
+    // the pair is computed if either tile is needed; the epilogue's mask makes
+    // the extra entries zero
+    ti.valid = (2 * mp * kBM < len) && (ti.n0 < corr_kbound(len, 2 * mp + 1, a.chunk));
     ti.nkb1 = cdiv(a.f, kBK);
   } else {
     const int ntA = cdiv(a.d, kBN);
-    const int nA = cdiv(a.glen, kBM) * ntA;
+    const int nA = cdiv(cdiv(a.glen, kBM), 2) * ntA;
     if (t < nA) {
-      const int m = t / ntA;
-      ti.m0 = m * kBM;
+      const int mp = t / ntA;
+      ti.m0 = (2 * mp + rank) * kBM;
       ti.n0 = (t % ntA) * kBN;
       ti.nkb1 = cdiv(a.f, kBK);
-      ti.nkb2 = corr_kbound(a.glen, m, a.chunk) / kBK;
+      // the correction range of the pair's lower tile; for its upper tile the
+      // extra blocks meet S entries that the Gram kernel masked to zero
+      ti.nkb2 = corr_kbound(a.glen, 2 * mp + 1, a.chunk) / kBK;
     } else {
       const int u = t - nA, ntU = cdiv(a.f, kBN);
       ti.kind = 1;
-      ti.m0 = (u / ntU) * kBM;
+      ti.m0 = (2 * (u / ntU) + rank) * kBM;
       ti.n0 = (u % ntU) * kBN;
       ti.npre = kWPreBlocks;
       ti.nkb1 = cdiv(a.glen, kBK);
@@ -181,12 +199,13 @@ __device__ __forceinline__ uint32_t kblock_bytes(const TileInfo& ti, int kb) {
   return kStageBytes;
 }
 
-// Issue the TMA loads of ring block `kb` of tile `ti` into stage buffers sa / sb
-// (for an update tile the first npre blocks are its fp32 W boxes, then the K
-// blocks of the MMA operands).
+// Issue this CTA's TMA loads of ring block `kb` of tile `ti` into stage
+// buffers sa / sb: its own A block, and its half (`rank`) of the pair's common
+// B block, multicast to both CTAs.  For an update tile the first npre blocks
+// are its own fp32 W boxes (not shared), then the K blocks of the operands.
 template <int MODE>
-__device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& ti, int kb,
-                                             uint8_t* sa, uint8_t* sb, uint64_t* bar) {
+__device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& ti, int kb, int rank,
+                                            uint8_t* sa, uint8_t* sb, uint64_t* bar) {
   if (MODE == kGroup && ti.kind == 1) {
     if (kb < ti.npre) {
       const int b0 = kb * kWBoxesPerStage, b1 = min(b0 + kWBoxesPerStage, kWBoxes);
@@ -196,28 +215,31 @@ __device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& t
     }
     kb -= ti.npre;
   }
+  const int kh = kBN / 2;  // B rows (or MN columns) per half
   if (MODE == kSwiGLU) {
     tma_load_2d(sa, &a.map[0], bar, kb * kBK, ti.m0);
-    tma_load_2d(sb, &a.map[1], bar, kb * kBK, ti.n0);
-    tma_load_2d(sb + kBBytes / 2, &a.map[2], bar, kb * kBK, ti.n0);
+    tma_load_2d_mc(sb + rank * (kBBytes / 2), &a.map[1 + rank], bar, kb * kBK, ti.n0, kPairMask);
   } else if (MODE == kVProj) {
     tma_load_2d(sa, &a.map[0], bar, kb * kBK, ti.m0);
-    tma_load_2d(sb, &a.map[1], bar, kb * kBK, ti.n0);
+    tma_load_2d_mc(sb + rank * (kBBytes / 2), &a.map[1], bar, kb * kBK, ti.n0 + rank * kh,
+                   kPairMask);
   } else if (MODE == kSGram) {
     const int gs = a.g_start[ti.g];
     tma_load_2d(sa, &a.map[0], bar, kb * kBK, gs + ti.m0);
-    tma_load_2d(sb, &a.map[1], bar, kb * kBK, gs + ti.n0);
+    tma_load_2d_mc(sb + rank * (kBBytes / 2), &a.map[1], bar, kb * kBK, gs + ti.n0 + rank * kh,
+                   kPairMask);
   } else {
     if (ti.kind == 0) {
       if (kb < ti.nkb1) {
         tma_load_2d(sa, &a.map[0], bar, kb * kBK, a.g0 + ti.m0);
-        tma_load_2d(sb, &a.map[1], bar, kb * kBK, ti.n0);
+        tma_load_2d_mc(sb + rank * (kBBytes / 2), &a.map[1], bar, kb * kBK, ti.n0 + rank * kh,
+                       kPairMask);
       } else {
         const int k2 = (kb - ti.nkb1) * kBK;
         tma_load_2d(sa, &a.map[2], bar, k2, a.gslot * a.s_pad + ti.m0);
 #pragma unroll
-        for (int q = 0; q < kBN / 64; ++q)
-          tma_load_2d(sb + q * 8192, &a.map[3], bar, ti.n0 + q * 64, a.g0 + k2);
+        for (int q = 2 * rank; q < 2 * rank + 2; ++q)
+          tma_load_2d_mc(sb + q * 8192, &a.map[3], bar, ti.n0 + q * 64, a.g0 + k2, kPairMask);
       }
     } else {
       const int k = a.g0 + kb * kBK;  // kb already excludes the preload blocks
@@ -225,8 +247,8 @@ __device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& t
       for (int q = 0; q < kBM / 64; ++q)
         tma_load_2d(sa + q * 8192, &a.map[4], bar, ti.m0 + q * 64, k);
 #pragma unroll
-      for (int q = 0; q < kBN / 64; ++q)
-        tma_load_2d(sb + q * 8192, &a.map[5], bar, ti.n0 + q * 64, k);
+      for (int q = 2 * rank; q < 2 * rank + 2; ++q)
+        tma_load_2d_mc(sb + q * 8192, &a.map[5], bar, ti.n0 + q * 64, k, kPairMask);
     }
   }
 }
@@ -380,6 +402,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the dynamic window starts at the same offset in every CTA, so aligning the
+  // same way keeps the layout (multicast targets, barriers) identical in both
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stage_base = smem;
@@ -389,7 +413,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   uint64_t* acc_full = empty + kStages;        // [2]
   uint64_t* acc_empty = acc_full + 2;          // [2]
   uint64_t* sched_full = acc_empty + 2;        // [kSchedRing]
-  uint64_t* sched_empty = sched_full + kSchedRing;  // [kSchedRing]
+  uint64_t* sched_empty = sched_full + kSchedRing;  // [kSchedRing] (the leader's counts)
   uint64_t* drain = sched_empty + kSchedRing;  // [1]
   int* sched_item = reinterpret_cast<int*>(drain + 1);  // [kSchedRing]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sched_item + kSchedRing);
@@ -399,11 +423,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int ntiles = num_tiles<MODE>(a);
+  const int rank = static_cast<int>(cluster_ctarank());
+  const bool leader = rank == 0;
+
+  // A consumer of scheduler slot `slot` releases it on the leader's barrier
+  // (the leader refills both CTAs' slots).
+  auto release_slot = [&](int slot) {
+    if (leader)
+      mbar_arrive(&sched_empty[slot]);
+    else
+      mbar_arrive_cluster(cluster_map(smem_u32(&sched_empty[slot]), 0));
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], 2);  // released by both CTAs' MMAs
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -411,7 +446,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     }
     for (int s = 0; s < kSchedRing; ++s) {
       mbar_init(&sched_full[s], 1);
-      mbar_init(&sched_empty[s], 5);
+      // leader: its MMA + 4 epilogue warps, and the peer's producer, MMA and
+      // 4 epilogue warps
+      mbar_init(&sched_empty[s], leader ? 11 : 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -423,12 +460,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer + tile scheduler
+      // ---------------- TMA producer (+ the pair's tile scheduler on the leader)
 #pragma unroll 1
       for (int q = 0; q < 7; ++q) tma_prefetch_desc(&a.map[q]);
       int stage = 0;
@@ -439,12 +477,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       for (int it = 0; ok; ++it) {
         const int slot = it % kSchedRing;
         const uint32_t sp = (it / kSchedRing) & 1;
-        if (!mbar_wait(&sched_empty[slot], sp ^ 1, abort_flag, a.err, kErrWaitSched)) break;
-        const int t = atomicAdd(a.counter, 1);
-        sched_item[slot] = t;
-        mbar_arrive(&sched_full[slot]);
+        int t;
+        if (leader) {
+          if (!mbar_wait(&sched_empty[slot], sp ^ 1, abort_flag, a.err, kErrWaitSched)) break;
+          t = atomicAdd(a.counter, 1);
+          sched_item[slot] = t;
+          st_cluster_u32(cluster_map(smem_u32(&sched_item[slot]), 1), static_cast<uint32_t>(t));
+          mbar_arrive(&sched_full[slot]);
+          mbar_arrive_cluster(cluster_map(smem_u32(&sched_full[slot]), 1));
+        } else {
+          if (!mbar_wait(&sched_full[slot], sp, abort_flag, a.err, kErrWaitSched)) break;
+          t = sched_item[slot];
+          release_slot(slot);
+        }
         if (t >= ntiles) break;
-        const TileInfo ti = decode_tile<MODE>(a, t);
+        const TileInfo ti = decode_tile<MODE>(a, t, rank);
         if (!ti.valid) continue;
         const int nkb = ti.npre + ti.nkb1 + ti.nkb2;
 #pragma unroll 1
@@ -455,7 +502,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           }
           uint8_t* sa = stage_base + stage * kStageBytes;
           mbar_arrive_expect_tx(&full[stage], kblock_bytes<MODE>(ti, kb));
-          load_kblock<MODE>(a, ti, kb, sa, sa + kABytes, &full[stage]);
+          load_kblock<MODE>(a, ti, kb, rank, sa, sa + kABytes, &full[stage]);
           ++fills;
           if (++stage == kStages) {
             stage = 0;
@@ -486,9 +533,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
                        kErrWaitSched))
           break;
         const int t = sched_item[slot];
-        mbar_arrive(&sched_empty[slot]);
+        release_slot(slot);
         if (t >= ntiles) break;
-        const TileInfo ti = decode_tile<MODE>(a, t);
+        const TileInfo ti = decode_tile<MODE>(a, t, rank);
         if (!ti.valid) continue;
         const int buf = acc_it & 1;
         if (!mbar_wait(&acc_empty[buf], ((acc_it >> 1) & 1) ^ 1, abort_flag, a.err,
@@ -529,7 +576,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
               tc_mma_bf16(tacc, ad, bd, idesc, (ti.npre > 0 || kk > 0 || k > 0) ? 1u : 0u);
             }
           }
-          tc_commit(&empty[stage]);
+          // the stage is free once both CTAs' MMAs have read it (the B halves
+          // live in both CTAs' copies of the stage)
+          tc_commit_mc(&empty[stage], kPairMask);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -539,11 +588,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         tc_commit(&acc_full[buf]);
         ++acc_it;
       }
-      if (*abort_flag) {
-        tc_commit(drain);
-        volatile int never = 0;
-        mbar_wait(drain, 0, &never, a.err, kErrWaitDrain);
-      }
+      // every tcgen05 op of this CTA (and the arrivals it signals in the peer)
+      // completes before the pair leaves
+      tc_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never, a.err, kErrWaitDrain);
     }
   } else {
     // ---------------- epilogue warps
@@ -562,9 +611,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       if (!ok) break;
       const int t = sched_item[slot];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sched_empty[slot]);
+      if (lane == 0) release_slot(slot);
       if (t >= ntiles) break;
-      const TileInfo ti = decode_tile<MODE>(a, t);
+      const TileInfo ti = decode_tile<MODE>(a, t, rank);
       if (!ti.valid) continue;
       const int buf = acc_it & 1;
       if (lane == 0)
@@ -583,6 +632,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // no remote arrival or multicast targets a CTA that has left
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);

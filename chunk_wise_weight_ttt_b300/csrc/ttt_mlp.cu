@@ -29,6 +29,7 @@ struct ttt_mlp {
   size_t ws_bytes;
   bool tc;
   int G, L, s_pad, s_slots, num_sms;
+  int max_pairs;            // co-resident CTA pairs of the tcgen05 kernels
   float* W;                 // n_docs x d x f
   __nv_bfloat16* Wb[2];     // bf16 operand copies of the current state
   __nv_bfloat16* WtT;       // W_target transposed (out x in)
@@ -226,12 +227,58 @@ std::vector<Span> plan_groups(int64_t n, int C, int G, const int64_t* ds, int nd
   return out;
 }
 
+int cdiv_h(int a, int b) { return (a + b - 1) / b; }
+
+// Launch the tcgen05 engine as clusters of two CTAs: one persistent cluster
+// per co-resident CTA pair, at most one per tile pair.
 template <int MODE>
-cudaError_t launch_gemm(ttt_mlp* h, GemmArgs& a, int ntiles, cudaStream_t st) {
-  if (ntiles <= 0) return cudaSuccess;
-  const int grid = std::max(1, std::min(h->num_sms, ntiles));
-  tc_gemm_kernel<MODE><<<grid, kGemmThreads, kGemmSmemBytes, st>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_pairs(int max_pairs, const GemmArgs& a, int npairs, cudaStream_t st) {
+  if (npairs <= 0) return cudaSuccess;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(2 * std::max(1, std::min(max_pairs, npairs)));
+  lc.blockDim = dim3(kGemmThreads);
+  lc.dynamicSmemBytes = kGemmSmemBytes;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, tc_gemm_kernel<MODE>, a);
+}
+
+template <int MODE>
+cudaError_t launch_gemm(ttt_mlp* h, GemmArgs& a, int npairs, cudaStream_t st) {
+  return launch_pairs<MODE>(h->max_pairs, a, npairs, st);
+}
+
+// Kernel attributes of the tcgen05 engine and the number of CTA pairs that can
+// be resident at once (0 on failure).
+cudaError_t setup_tc_kernels(int* max_pairs) {
+  const void* kfn[4] = {(const void*)tc_gemm_kernel<kSwiGLU>, (const void*)tc_gemm_kernel<kVProj>,
+                        (const void*)tc_gemm_kernel<kSGram>, (const void*)tc_gemm_kernel<kGroup>};
+  for (const void* k : kfn) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(2);
+  lc.blockDim = dim3(kGemmThreads);
+  lc.dynamicSmemBytes = kGemmSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  int n = 0;
+  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, (const void*)tc_gemm_kernel<kGroup>, &lc);
+  if (e != cudaSuccess) return e;
+  *max_pairs = n;
+  return n > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
 // Phase timing (only while profiling is enabled): an event pair per phase.
@@ -273,7 +320,7 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
   if (!make_map(&map_x, x, d, n, d, 64, 128, &why) ||
       !make_map(&map_u, h->U, d, n, d, 64, 128, &why) ||
       !make_map(&map_za, h->Z, f, n, f, 64, 128, &why) ||
-      !make_map(&map_zb, h->Z, f, n, f, 64, 256, &why) ||
+      !make_map(&map_zb, h->Z, f, n, f, 64, 128, &why) ||
       !make_map(&map_vmn, h->V, d, n, d, 64, 64, &why) ||
       !make_map(&map_zmn, h->Z, f, n, f, 64, 64, &why))
     return fail(h, TTT_ECUDA, why);
@@ -319,7 +366,7 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
   a.out0 = h->Z;
   a.counter = next_counter(h, st);
   pt.begin(1);
-  TTT_CK(h, launch_gemm<kSwiGLU>(h, a, ((int)n + kBM - 1) / kBM * ((f + kBM - 1) / kBM), st));
+  TTT_CK(h, launch_gemm<kSwiGLU>(h, a, cdiv_h(cdiv_h((int)n, kBM), 2) * cdiv_h(f, kBM), st));
   pt.end();
   h->prof_launches++;
 
@@ -330,7 +377,7 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
   a.alpha = c.eta;
   a.counter = next_counter(h, st);
   pt.begin(2);
-  TTT_CK(h, launch_gemm<kVProj>(h, a, ((int)n + kBM - 1) / kBM * ((d + kBN - 1) / kBN), st));
+  TTT_CK(h, launch_gemm<kVProj>(h, a, cdiv_h(cdiv_h((int)n, kBM), 2) * cdiv_h(d, kBN), st));
   pt.end();
   h->prof_launches++;
 
@@ -358,7 +405,7 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
     s.map[1] = map_zb;
     s.out0 = h->S;
     s.counter = next_counter(h, st);
-    const int per = ((h->s_pad + kBM - 1) / kBM) * ((h->s_pad + kBN - 1) / kBN);
+    const int per = cdiv_h(cdiv_h(h->s_pad, kBM), 2) * cdiv_h(h->s_pad, kBN);
     if (h->G > 1) {
       pt.begin(3);
       TTT_CK(h, launch_gemm<kSGram>(h, s, s.n_groups * per, st));
@@ -405,8 +452,8 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
       q.glen = g.len;
       q.gslot = (int)(i - w0);
       q.counter = next_counter(h, st);
-      const int nt = ((g.len + kBM - 1) / kBM) * ((d + kBN - 1) / kBN) +
-                     ((d + kBM - 1) / kBM) * ((f + kBN - 1) / kBN);
+      const int nt = cdiv_h(cdiv_h(g.len, kBM), 2) * cdiv_h(d, kBN) +
+                     cdiv_h(cdiv_h(d, kBM), 2) * cdiv_h(f, kBN);
       TTT_CK(h, launch_gemm<kGroup>(h, q, nt, st));
       h->prof_launches++;
       h->prof_group_launches++;
@@ -611,18 +658,16 @@ ttt_status ttt_mlp_create(const ttt_mlp_config* cfg, const void* w_gate, const v
     const int d = cfg->d, f = cfg->f;
     if (!make_map(&h->map_wg, w_gate, d, f, d, 64, 128, &why) ||
         !make_map(&h->map_wu, w_up, d, f, d, 64, 128, &why) ||
-        !make_map(&h->map_wtT, h->WtT, d, d, d, 64, 256, &why) ||
+        !make_map(&h->map_wtT, h->WtT, d, d, d, 64, 128, &why) ||
         !make_map(&h->map_s, h->S, h->s_pad, (uint64_t)h->s_slots * h->s_pad, h->s_pad, 64, 128, &why) ||
-        !make_map(&h->map_w0, w_down0, f, d, f, 64, 256, &why) ||
-        !make_map(&h->map_wb[0], h->Wb[0], f, d, f, 64, 256, &why) ||
-        !make_map(&h->map_wb[1], h->Wb[1], f, d, f, 64, 256, &why))
+        !make_map(&h->map_w0, w_down0, f, d, f, 64, 128, &why) ||
+        !make_map(&h->map_wb[0], h->Wb[0], f, d, f, 64, 128, &why) ||
+        !make_map(&h->map_wb[1], h->Wb[1], f, d, f, 64, 128, &why))
       return bail(TTT_ECUDA, why);
-    const void* kfn[4] = {(const void*)tc_gemm_kernel<kSwiGLU>, (const void*)tc_gemm_kernel<kVProj>,
-                          (const void*)tc_gemm_kernel<kSGram>, (const void*)tc_gemm_kernel<kGroup>};
-    for (const void* k : kfn) {
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
-      if (e != cudaSuccess) return bail(TTT_ECUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-    }
+    e = setup_tc_kernels(&h->max_pairs);
+    if (e != cudaSuccess)
+      return bail(TTT_ECUDA, std::string("tcgen05 kernel set-up (attributes, cluster occupancy): ") +
+                                 cudaGetErrorString(e));
     dim3 tb(32, 8), tg((d + 31) / 32, (d + 31) / 32);
     transpose_kernel<__nv_bfloat16><<<tg, tb, 0, st>>>((const __nv_bfloat16*)w_target, h->WtT, d, d);
     e = cudaGetLastError();
@@ -813,29 +858,26 @@ namespace {
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 unsigned char* g_noalloc_ptr[kNoallocMaxDevices] = {};
-int g_noalloc_sms[kNoallocMaxDevices] = {};
+int g_noalloc_pairs[kNoallocMaxDevices] = {};
 
-// One-time set-up of the current device: scratch address and kernel attributes.
-ttt_status noalloc_setup(int dev, unsigned char** ptr, int* sms) {
+// One-time set-up of the current device: scratch address, kernel attributes
+// and the number of co-resident CTA pairs.
+ttt_status noalloc_setup(int dev, unsigned char** ptr, int* pairs_out) {
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_ptr[dev]) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess)
       return fail(nullptr, TTT_ECUDA, std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e));
-    e = cudaFuncSetAttribute((const void*)tc_gemm_kernel<kVProj>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+    int pairs = 0;
+    e = setup_tc_kernels(&pairs);
     if (e != cudaSuccess)
-      return fail(nullptr, TTT_ECUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-    int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess)
-      return fail(nullptr, TTT_ECUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
-    g_noalloc_sms[dev] = n;
+      return fail(nullptr, TTT_ECUDA, std::string("tcgen05 kernel set-up: ") + cudaGetErrorString(e));
+    g_noalloc_pairs[dev] = pairs;
     g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
   }
   *ptr = g_noalloc_ptr[dev];
-  *sms = g_noalloc_sms[dev];
+  *pairs_out = g_noalloc_pairs[dev];
   return TTT_OK;
 }
 
@@ -872,8 +914,8 @@ extern "C" ttt_status ttt_target_noalloc(const void* x0, const void* conv_w, con
   TTT_CK(nullptr, cudaGetDevice(&dev));
   if (dev < 0 || dev >= kNoallocMaxDevices) return fail(nullptr, TTT_EUNSUPPORTED, "ttt_target_noalloc: device ordinal too large");
   unsigned char* scratch = nullptr;
-  int sms = 0;
-  ttt_status s = noalloc_setup(dev, &scratch, &sms);
+  int pairs = 0;
+  ttt_status s = noalloc_setup(dev, &scratch, &pairs);
   if (s != TTT_OK) return s;
 
   // scratch layout: [0,256) control (tile counter, error word) | W_target^T | U
@@ -909,7 +951,7 @@ extern "C" ttt_status ttt_target_noalloc(const void* x0, const void* conv_w, con
   GemmArgs a;
   std::memset(&a, 0, sizeof a);
   if (!make_map(&a.map[0], u, d, n_tokens, d, 64, 128, &why) ||
-      !make_map(&a.map[1], wtT, d, d, d, 64, 256, &why))
+      !make_map(&a.map[1], wtT, d, d, d, 64, 128, &why))
     return fail(nullptr, TTT_ECUDA, why);
   a.n_rows = (int)n_tokens;
   a.d = d;
@@ -919,8 +961,7 @@ extern "C" ttt_status ttt_target_noalloc(const void* x0, const void* conv_w, con
   a.counter = ctrl;
   a.err = err;
   a.out0 = v;
-  const int ntiles = ((int)n_tokens + kBM - 1) / kBM * ((d + kBN - 1) / kBN);
-  tc_gemm_kernel<kVProj><<<std::max(1, std::min(sms, ntiles)), kGemmThreads, kGemmSmemBytes, st>>>(a);
-  TTT_CK(nullptr, cudaGetLastError());
+  const int npairs = cdiv_h(cdiv_h((int)n_tokens, kBM), 2) * cdiv_h(d, kBN);
+  TTT_CK(nullptr, launch_pairs<kVProj>(pairs, a, npairs, st));
   return TTT_OK;
 }
