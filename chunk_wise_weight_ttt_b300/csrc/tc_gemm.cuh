@@ -1,19 +1,22 @@
 // Persistent, warp-specialised tcgen05 GEMM engine for the bf16 hot path.
 //
-// CTAs run in clusters of two (one CTA per SM).  The pair works on two
-// vertically adjacent 128x256 tiles that share their B operand: each CTA loads
-// its own A block and one half of the common B block, which TMA multicasts into
-// both CTAs' shared memory, so a CTA reads 32 of the 48 KB of every ring stage
-// from L2.  The leader CTA (rank 0) claims tile pairs from a dynamic counter
-// and hands each to its peer through distributed shared memory; a ring stage is
-// refilled only after both CTAs' MMAs have released it.
+// CTAs run in clusters of two (one CTA per SM) that compute one 256x256 tile
+// with the pair form of the 5th-generation MMA (tcgen05 cta_group::2): CTA r
+// holds rows [128r, 128r+128) of the A block and of the B block (B's N half)
+// in its shared memory, the even CTA issues the MMAs for both, and each CTA's
+// TMEM receives its 128 accumulator rows.  A ring stage is therefore 32 KB per
+// CTA (6 stages) and carries 1.5x the MMA work per byte of a 128x256 tile.
+// The even CTA (the leader) claims tiles from a dynamic counter and hands each
+// to its peer through distributed shared memory; both CTAs' TMA loads signal
+// the leader's ring barriers, and the leader's commits release the stages and
+// accumulators in both CTAs.
 //
 // Each CTA has 192 threads:
-//   warp 0      TMA producer: streams the operand blocks (64 K-elements each)
-//               of the CTA's tile into a 4-stage shared-memory ring with
-//               128-byte swizzle.
+//   warp 0      TMA producer: streams this CTA's operand halves (64 K-elements
+//               per block) into its shared-memory ring with 128-byte swizzle.
 //   warp 1      owns the TMEM allocation (512 columns = two 128x256 fp32
-//               accumulators) and issues tcgen05.mma from one thread.
+//               accumulators, allocated together with the peer) and, in the
+//               leader, issues the pair's tcgen05.mma from one thread.
 //   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (one TMEM
 //               lane = one output row per thread), the mode's arithmetic, and
 //               global stores; the other accumulator is filled meanwhile.
@@ -30,7 +33,7 @@
 //            and the update tiles
 //              W <- W_s + V_g^T Z_g,  Wb_next <- bf16(W)
 //            in one launch.  An update tile first streams its fp32 block of
-//            W_s through the operand ring into the TMEM accumulator
+//            W_s through the operand ring into the TMEM accumulators
 //            (tcgen05.cp), so the MMAs accumulate straight onto the fast
 //            weight and the epilogue only stores (W and its bf16 copy),
 //            coalesced through a per-warp shared-memory transpose.
@@ -51,10 +54,10 @@ namespace ttt {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
-constexpr int kABytes = kBM * kBK * 2;          // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
+constexpr int kStages = 6;
+constexpr int kABytes = kBM * kBK * 2;            // 16 KB: this CTA's 128 A rows
+constexpr int kBHalfBytes = (kBN / 2) * kBK * 2;  // 16 KB: this CTA's 128 B rows
+constexpr int kStageBytes = kABytes + kBHalfBytes;  // 32 KB per CTA
 constexpr int kTmemCols = 2 * kBN;              // two fp32 accumulators
 constexpr int kSchedRing = 4;
 constexpr int kGemmThreads = 192;
@@ -62,7 +65,7 @@ constexpr int kMaxGroups = 256;
 constexpr int kSwizzlePairs = 8;   // SwiGLU raster: tile pairs per column sweep
 constexpr uint16_t kPairMask = 0x3;  // both CTAs of the cluster
 // fp32 fast-weight preload of an update tile: boxes of 32 columns x 128 rows
-// (128-byte rows, 16 KB), three per ring stage.
+// (128-byte rows, 16 KB), two per ring stage.
 constexpr int kWBoxCols = 32;
 constexpr int kWBoxBytes = kBM * kWBoxCols * 4;
 constexpr int kWBoxesPerStage = kStageBytes / kWBoxBytes;
@@ -74,7 +77,7 @@ constexpr int kEpiWarps = 4;
 
 enum GemmMode : int { kSwiGLU = 0, kVProj = 1, kSGram = 2, kGroup = 3 };
 
-// Tensor-map slots per mode (B boxes are the half that one CTA of a pair loads).
+// Tensor-map slots per mode (B boxes are the half that one CTA of a pair holds).
 //   kSwiGLU: 0 X (box 64x128), 1 Wg (64x128), 2 Wu (64x128)
 //   kVProj:  0 U (64x128), 1 W_target^T (64x128)
 //   kSGram:  0 Z (64x128), 1 Z (64x128)
@@ -191,64 +194,64 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int ra
   return ti;
 }
 
-// Bytes that ring block `kb` of tile `ti` brings in.
+// Bytes that ring block `kb` of the pair's tiles brings into both CTAs (what
+// the leader's full barrier expects).
 template <int MODE>
 __device__ __forceinline__ uint32_t kblock_bytes(const TileInfo& ti, int kb) {
   if (MODE == kGroup && kb < ti.npre)
-    return static_cast<uint32_t>(min(kWBoxesPerStage, kWBoxes - kb * kWBoxesPerStage)) * kWBoxBytes;
-  return kStageBytes;
+    return 2u * static_cast<uint32_t>(min(kWBoxesPerStage, kWBoxes - kb * kWBoxesPerStage)) *
+           kWBoxBytes;
+  return 2u * kStageBytes;
 }
 
 // Issue this CTA's TMA loads of ring block `kb` of tile `ti` into stage
-// buffers sa / sb: its own A block, and its half (`rank`) of the pair's common
-// B block, multicast to both CTAs.  For an update tile the first npre blocks
-// are its own fp32 W boxes (not shared), then the K blocks of the operands.
+// buffers sa / sb: its A rows and its half (`rank`) of the B block, with
+// completion signalled on the leader's barrier `bar` (a shared::cluster
+// address).  For an update tile the first npre blocks are this CTA's fp32 W
+// boxes, then the K blocks of the operands.
 template <int MODE>
 __device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& ti, int kb, int rank,
-                                            uint8_t* sa, uint8_t* sb, uint64_t* bar) {
+                                            uint8_t* sa, uint8_t* sb, uint32_t bar) {
   if (MODE == kGroup && ti.kind == 1) {
     if (kb < ti.npre) {
       const int b0 = kb * kWBoxesPerStage, b1 = min(b0 + kWBoxesPerStage, kWBoxes);
       for (int b = b0; b < b1; ++b)
-        tma_load_2d(sa + (b - b0) * kWBoxBytes, &a.map[6], bar, ti.n0 + b * kWBoxCols, ti.m0);
+        tma_load_2d_pair(sa + (b - b0) * kWBoxBytes, &a.map[6], bar, ti.n0 + b * kWBoxCols, ti.m0);
       return;
     }
     kb -= ti.npre;
   }
   const int kh = kBN / 2;  // B rows (or MN columns) per half
   if (MODE == kSwiGLU) {
-    tma_load_2d(sa, &a.map[0], bar, kb * kBK, ti.m0);
-    tma_load_2d_mc(sb + rank * (kBBytes / 2), &a.map[1 + rank], bar, kb * kBK, ti.n0, kPairMask);
+    tma_load_2d_pair(sa, &a.map[0], bar, kb * kBK, ti.m0);
+    tma_load_2d_pair(sb, &a.map[1 + rank], bar, kb * kBK, ti.n0);
   } else if (MODE == kVProj) {
-    tma_load_2d(sa, &a.map[0], bar, kb * kBK, ti.m0);
-    tma_load_2d_mc(sb + rank * (kBBytes / 2), &a.map[1], bar, kb * kBK, ti.n0 + rank * kh,
-                   kPairMask);
+    tma_load_2d_pair(sa, &a.map[0], bar, kb * kBK, ti.m0);
+    tma_load_2d_pair(sb, &a.map[1], bar, kb * kBK, ti.n0 + rank * kh);
   } else if (MODE == kSGram) {
     const int gs = a.g_start[ti.g];
-    tma_load_2d(sa, &a.map[0], bar, kb * kBK, gs + ti.m0);
-    tma_load_2d_mc(sb + rank * (kBBytes / 2), &a.map[1], bar, kb * kBK, gs + ti.n0 + rank * kh,
-                   kPairMask);
+    tma_load_2d_pair(sa, &a.map[0], bar, kb * kBK, gs + ti.m0);
+    tma_load_2d_pair(sb, &a.map[1], bar, kb * kBK, gs + ti.n0 + rank * kh);
   } else {
     if (ti.kind == 0) {
       if (kb < ti.nkb1) {
-        tma_load_2d(sa, &a.map[0], bar, kb * kBK, a.g0 + ti.m0);
-        tma_load_2d_mc(sb + rank * (kBBytes / 2), &a.map[1], bar, kb * kBK, ti.n0 + rank * kh,
-                       kPairMask);
+        tma_load_2d_pair(sa, &a.map[0], bar, kb * kBK, a.g0 + ti.m0);
+        tma_load_2d_pair(sb, &a.map[1], bar, kb * kBK, ti.n0 + rank * kh);
       } else {
         const int k2 = (kb - ti.nkb1) * kBK;
-        tma_load_2d(sa, &a.map[2], bar, k2, a.gslot * a.s_pad + ti.m0);
+        tma_load_2d_pair(sa, &a.map[2], bar, k2, a.gslot * a.s_pad + ti.m0);
 #pragma unroll
-        for (int q = 2 * rank; q < 2 * rank + 2; ++q)
-          tma_load_2d_mc(sb + q * 8192, &a.map[3], bar, ti.n0 + q * 64, a.g0 + k2, kPairMask);
+        for (int q = 0; q < 2; ++q)
+          tma_load_2d_pair(sb + q * 8192, &a.map[3], bar, ti.n0 + rank * kh + q * 64, a.g0 + k2);
       }
     } else {
       const int k = a.g0 + kb * kBK;  // kb already excludes the preload blocks
 #pragma unroll
       for (int q = 0; q < kBM / 64; ++q)
-        tma_load_2d(sa + q * 8192, &a.map[4], bar, ti.m0 + q * 64, k);
+        tma_load_2d_pair(sa + q * 8192, &a.map[4], bar, ti.m0 + q * 64, k);
 #pragma unroll
-      for (int q = 2 * rank; q < 2 * rank + 2; ++q)
-        tma_load_2d_mc(sb + q * 8192, &a.map[5], bar, ti.n0 + q * 64, k, kPairMask);
+      for (int q = 0; q < 2; ++q)
+        tma_load_2d_pair(sb + q * 8192, &a.map[5], bar, ti.n0 + rank * kh + q * 64, k);
     }
   }
 }
@@ -403,17 +406,17 @@ template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the dynamic window starts at the same offset in every CTA, so aligning the
-  // same way keeps the layout (multicast targets, barriers) identical in both
+  // same way keeps the layout (MMA operand halves, barriers) identical in both
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stage_base = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint64_t* full = bars;                       // [kStages]
+  uint64_t* full = bars;                       // [kStages]  (used in the leader)
   uint64_t* empty = full + kStages;            // [kStages]
   uint64_t* acc_full = empty + kStages;        // [2]
-  uint64_t* acc_empty = acc_full + 2;          // [2]
+  uint64_t* acc_empty = acc_full + 2;          // [2]        (used in the leader)
   uint64_t* sched_full = acc_empty + 2;        // [kSchedRing]
-  uint64_t* sched_empty = sched_full + kSchedRing;  // [kSchedRing] (the leader's counts)
+  uint64_t* sched_empty = sched_full + kSchedRing;  // [kSchedRing] (used in the leader)
   uint64_t* drain = sched_empty + kSchedRing;  // [1]
   int* sched_item = reinterpret_cast<int*>(drain + 1);  // [kSchedRing]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sched_item + kSchedRing);
@@ -426,41 +429,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   const int rank = static_cast<int>(cluster_ctarank());
   const bool leader = rank == 0;
 
-  // A consumer of scheduler slot `slot` releases it on the leader's barrier
-  // (the leader refills both CTAs' slots).
-  auto release_slot = [&](int slot) {
+  // Arrive on the leader's copy of a barrier (local in the leader, remote in the peer).
+  auto arrive_leader = [&](uint64_t* bar) {
     if (leader)
-      mbar_arrive(&sched_empty[slot]);
+      mbar_arrive(bar);
     else
-      mbar_arrive_cluster(cluster_map(smem_u32(&sched_empty[slot]), 0));
+      mbar_arrive_cluster(cluster_map(smem_u32(bar), 0));
   };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 2);  // released by both CTAs' MMAs
+      mbar_init(&full[s], 1);   // the leader's expect; both CTAs' bytes
+      mbar_init(&empty[s], 1);  // the leader's MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], 2 * kEpiWarps);  // both CTAs' epilogue warps
     }
     for (int s = 0; s < kSchedRing; ++s) {
       mbar_init(&sched_full[s], 1);
-      // leader: its MMA + 4 epilogue warps, and the peer's producer, MMA and
-      // 4 epilogue warps
-      mbar_init(&sched_empty[s], leader ? 11 : 1);
+      // leader: its MMA + epilogue warps, and the peer's producer + epilogue warps
+      mbar_init(&sched_empty[s], 2 + 2 * kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // both CTAs' barriers exist before any remote arrival
+  cluster_sync_all();  // both CTAs' barriers and TMEM exist before any pair traffic
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -488,7 +489,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         } else {
           if (!mbar_wait(&sched_full[slot], sp, abort_flag, a.err, kErrWaitSched)) break;
           t = sched_item[slot];
-          release_slot(slot);
+          arrive_leader(&sched_empty[slot]);
         }
         if (t >= ntiles) break;
         const TileInfo ti = decode_tile<MODE>(a, t, rank);
@@ -501,8 +502,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             break;
           }
           uint8_t* sa = stage_base + stage * kStageBytes;
-          mbar_arrive_expect_tx(&full[stage], kblock_bytes<MODE>(ti, kb));
-          load_kblock<MODE>(a, ti, kb, rank, sa, sa + kABytes, &full[stage]);
+          if (leader) mbar_arrive_expect_tx(&full[stage], kblock_bytes<MODE>(ti, kb));
+          load_kblock<MODE>(a, ti, kb, rank, sa, sa + kABytes, cluster_map(smem_u32(&full[stage]), 0));
           ++fills;
           if (++stage == kStages) {
             stage = 0;
@@ -510,7 +511,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           }
         }
       }
-      if (*abort_flag) {
+      if (*abort_flag && leader) {
         // let every load still in flight land before the CTA's smem is released
         for (int s = 0; s < kStages && s < fills; ++s) {
           const uint32_t p = (s < stage) ? phase : (phase ^ 1);
@@ -520,8 +521,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer for the pair
       int stage = 0;
       uint32_t phase = 0;
       int acc_it = 0;
@@ -533,7 +534,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
                        kErrWaitSched))
           break;
         const int t = sched_item[slot];
-        release_slot(slot);
+        mbar_arrive(&sched_empty[slot]);
         if (t >= ntiles) break;
         const TileInfo ti = decode_tile<MODE>(a, t, rank);
         if (!ti.valid) continue;
@@ -553,44 +554,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           tc_fence_after();
           const uint32_t sa = smem_u32(stage_base + stage * kStageBytes);
           if (kb < ti.npre) {
-            // fp32 W boxes (128 rows x 128 B, 128-byte swizzle) -> accumulator
-            // columns, 8 columns per copy
+            // fp32 W boxes (128 rows x 128 B, 128-byte swizzle) -> each CTA's
+            // accumulator columns, 8 columns per copy
             const int b0 = kb * kWBoxesPerStage, b1 = min(b0 + kWBoxesPerStage, kWBoxes);
             for (int b = b0; b < b1; ++b) {
               const uint32_t src = sa + (b - b0) * kWBoxBytes;
 #pragma unroll
               for (int j = 0; j < kWBoxCols / 8; ++j)
-                tc_cp_128x256b(tacc + b * kWBoxCols + j * 8, sdesc_sw128(src + j * 32, 0, 1024));
+                tc_cp_128x256b_pair(tacc + b * kWBoxCols + j * 8, sdesc_sw128(src + j * 32, 0, 1024));
             }
           } else {
             const int kk = kb - ti.npre;
             const uint32_t sb = sa + kABytes;
             const int lay = kblock_layout<MODE>(ti, kk);
-            const uint32_t idesc = idesc_bf16_f32(kBM, kBN, lay == 2, lay >= 1);
+            const uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, lay == 2, lay >= 1);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
               const uint64_t ad = (lay == 2) ? sdesc_sw128(sa + k * 2048, 8192, 1024)
                                              : sdesc_sw128(sa + k * 32, 0, 1024);
               const uint64_t bd = (lay >= 1) ? sdesc_sw128(sb + k * 2048, 8192, 1024)
                                              : sdesc_sw128(sb + k * 32, 0, 1024);
-              tc_mma_bf16(tacc, ad, bd, idesc, (ti.npre > 0 || kk > 0 || k > 0) ? 1u : 0u);
+              tc_mma_bf16_pair(tacc, ad, bd, idesc, (ti.npre > 0 || kk > 0 || k > 0) ? 1u : 0u);
             }
           }
-          // the stage is free once both CTAs' MMAs have read it (the B halves
-          // live in both CTAs' copies of the stage)
-          tc_commit_mc(&empty[stage], kPairMask);
+          // the stage is free in both CTAs once the pair's MMAs have read it
+          tc_commit_pair_mc(&empty[stage], kPairMask);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        tc_commit(&acc_full[buf]);
+        tc_commit_pair_mc(&acc_full[buf], kPairMask);
         ++acc_it;
       }
-      // every tcgen05 op of this CTA (and the arrivals it signals in the peer)
-      // completes before the pair leaves
-      tc_commit(drain);
+      // every tcgen05 op of the pair (and the arrivals it signals) completes
+      // before the pair leaves
+      tc_commit_pair(drain);
       volatile int never = 0;
       mbar_wait(drain, 0, &never, a.err, kErrWaitDrain);
     }
@@ -611,7 +611,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       if (!ok) break;
       const int t = sched_item[slot];
       __syncwarp();
-      if (lane == 0) release_slot(slot);
+      if (lane == 0) arrive_leader(&sched_empty[slot]);
       if (t >= ntiles) break;
       const TileInfo ti = decode_tile<MODE>(a, t, rank);
       if (!ti.valid) continue;
@@ -625,17 +625,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       epilogue_tile<MODE>(a, ti, tacc, row, staging + (warp - 2) * kStgBytesPerWarp);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (lane == 0) arrive_leader(&acc_empty[buf]);
       ++acc_it;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // no remote arrival or multicast targets a CTA that has left
+  cluster_sync_all();  // no pair traffic targets a CTA that has left
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
