@@ -43,11 +43,13 @@ class TTTMLP:
 
     Weights are CUDA tensors in nn.Linear layouts (w_gate, w_up: f x d;
     w_down0: d x f) plus conv_w (k x d) and w_target (d x d, in x out).  The
-    object keeps references to the weights and owns its workspace tensor.
+    object keeps references to the weights and owns its workspace tensor, or
+    borrows `workspace` (a uint8 CUDA tensor of at least workspace_bytes())
+    when one is given.
     """
 
     def __init__(self, w_gate, w_up, w_down0, conv_w, w_target, *, chunk: int, eta: float,
-                 n_docs: int = 1, max_tokens: int, stream=None):
+                 n_docs: int = 1, max_tokens: int, stream=None, workspace=None):
         self.lib = _abi.load()
         dt = w_gate.dtype
         if dt not in _DT:
@@ -63,7 +65,11 @@ class TTTMLP:
         nbytes = self.lib.ttt_mlp_workspace_bytes(C.byref(self.cfg))
         if nbytes == 0:
             raise TTTError(_abi.TTT_EINVAL, "invalid configuration")
-        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=w_gate.device)
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=w_gate.device)
+        elif workspace.dtype != torch.uint8 or workspace.numel() < nbytes or not workspace.is_cuda:
+            raise ValueError(f"workspace must be a CUDA uint8 tensor of at least {nbytes} bytes")
+        self.workspace = workspace
         self._weights = ws
         h = C.c_void_p()
         st = self.lib.ttt_mlp_create(C.byref(self.cfg), *[_ptr(t) for t in ws], _ptr(self.workspace),
@@ -159,6 +165,65 @@ class TTTMLP:
             self.close()
         except Exception:
             pass
+
+
+def workspace_bytes(d: int, f: int, *, chunk: int, conv_k: int, dtype=torch.bfloat16,
+                    n_docs: int = 1, max_tokens: int, eta: float = 0.0) -> int:
+    """Device workspace (bytes) a layer of this shape needs."""
+    lib = _abi.load()
+    cfg = Config(d=d, f=f, chunk=chunk, conv_k=conv_k, n_docs=n_docs, eta=eta, act_dtype=_DT[dtype],
+                 max_tokens=max_tokens)
+    return int(lib.ttt_mlp_workspace_bytes(C.byref(cfg)))
+
+
+class TTTStack:
+    """Pre-norm residual stack of SwiGLU MLP blocks whose down projections are
+    In-Place TTT fast weights (no attention):
+        h_{l+1} = h_l + TTT_MLP_l(RMSNorm(h_l)),   X0 = h_0 for every layer.
+    Layer-major: each layer runs its chunk recursion over the whole call before
+    the next layer starts (the recursion is per layer and nothing else mixes
+    tokens).  All layers share one workspace, so a call processes whole
+    documents: its fast weights start at W_0 (doc_starts must contain 0) and
+    are not kept across calls.
+
+    layers: list of dicts with CUDA tensors w_gate, w_up, w_down0, conv_w,
+    w_target (one dtype).  h is fp32 (T x d); activations are cast to the
+    weights' dtype.
+    """
+
+    def __init__(self, layers, *, chunk: int, eta: float, max_tokens: int, eps: float = 1e-6):
+        self.layers = layers
+        w = layers[0]
+        self.dtype = w["w_gate"].dtype
+        f, d = w["w_gate"].shape
+        self.d, self.f, self.k = d, f, w["conv_w"].shape[0]
+        self.chunk, self.eta, self.max_tokens, self.eps = chunk, eta, max_tokens, eps
+        nbytes = workspace_bytes(d, f, chunk=chunk, conv_k=self.k, dtype=self.dtype,
+                                 max_tokens=max_tokens, eta=eta)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=w["w_gate"].device)
+
+    def forward(self, h0: torch.Tensor, doc_starts: Sequence[int] = (0,), stream=None,
+                n_layers: Optional[int] = None) -> torch.Tensor:
+        if not doc_starts or int(doc_starts[0]) != 0:
+            raise ValueError("a stack call processes whole documents: doc_starts must start with 0")
+        if h0.dtype != torch.float32 or h0.dim() != 2 or h0.shape[1] != self.d:
+            raise ValueError("h0 must be a float32 (T x d) CUDA tensor")
+        h = h0.clone()
+        x0 = h0.to(self.dtype)
+        x = torch.empty(h0.shape, dtype=self.dtype, device=h0.device)
+        o = torch.empty_like(x)
+        for w in self.layers[: n_layers or len(self.layers)]:
+            rmsnorm(h, x, self.eps, stream=stream)
+            layer = TTTMLP(w["w_gate"], w["w_up"], w["w_down0"], w["conv_w"], w["w_target"],
+                           chunk=self.chunk, eta=self.eta, max_tokens=self.max_tokens,
+                           stream=stream, workspace=self.workspace)
+            layer.forward(x, x0, doc_starts=doc_starts, out=o, stream=stream)
+            layer.check(stream=stream)
+            layer.close()
+            residual_add(h, o, stream=stream)
+        return h
+
+    __call__ = forward
 
 
 def rmsnorm(h: torch.Tensor, out: torch.Tensor, eps: float = 1e-6, stream=None) -> torch.Tensor:

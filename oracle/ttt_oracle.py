@@ -148,13 +148,14 @@ def ttt_layer(x, x0, w_gate, w_up, w_down0, conv_w, w_target, eta, chunk,
 
 
 def ttt_layer_rows(x, x0, w_gate, w_up, w_down0, conv_w, w_target, eta, chunk,
-                   rows, doc_starts=(0,), w_init=None):
+                   rows, doc_starts=(0,), w_init=None, z=None):
     """The same recursion restricted to a subset of W's rows.
 
     Row i of W, and column i of O, depend on all of Z but only on column i of
     V (W[i] += eta * sum_t V[t,i] Z[t]; O[t,i] = Z[t] . W[i]).  So the sampled
-    rows are exact without computing the others.  Returns (O[:, rows],
-    W[rows])."""
+    rows are exact without computing the others.  ``z`` may pass in
+    swiglu_intermediate(x, w_gate, w_up) when several runs share the tokens (Z
+    does not depend on the chunking or on W).  Returns (O[:, rows], W[rows])."""
     rows = np.asarray(rows, dtype=np.int64)
     x = _f64(x)
     x0 = _f64(x0)
@@ -166,10 +167,10 @@ def ttt_layer_rows(x, x0, w_gate, w_up, w_down0, conv_w, w_target, eta, chunk,
     for s, e, reset in chunk_spans(n, chunk, doc_starts):
         if reset:
             W = w0r.copy()
-        z = swiglu_intermediate(x[s:e], w_gate, w_up)
-        out[s:e] = z @ W.T
+        zc = swiglu_intermediate(x[s:e], w_gate, w_up) if z is None else _f64(z[s:e])
+        out[s:e] = zc @ W.T
         v = chunk_target_source(x0[s:e], conv_w) @ wt
-        W = W + float(eta) * (v.T @ z)
+        W = W + float(eta) * (v.T @ zc)
     return out, W
 
 

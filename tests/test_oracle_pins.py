@@ -303,6 +303,14 @@ def test_row_sampled_equals_full():
                                     cfg["chunk"], rows, cfg["doc_starts"])
     assert _rel(orow, o[:, rows]) < 1e-13
     assert _rel(wrow, w[rows]) < 1e-13
+    # a precomputed Z (from the torch library MLP) gives the same rows
+    x = _t(cfg["x"])
+    z = (F.silu(F.linear(x, _t(cfg["w_gate"]))) * F.linear(x, _t(cfg["w_up"]))).numpy()
+    orow2, wrow2 = orc.ttt_layer_rows(cfg["x"], cfg["x0"], cfg["w_gate"], cfg["w_up"],
+                                      cfg["w_down0"], cfg["conv_w"], cfg["w_target"], cfg["eta"],
+                                      cfg["chunk"], rows, cfg["doc_starts"], z=z)
+    assert _rel(orow2, o[:, rows]) < 1e-13
+    assert _rel(wrow2, w[rows]) < 1e-13
 
 
 def test_stack_matches_brute_force_composition():

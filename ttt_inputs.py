@@ -18,7 +18,12 @@ then cast).  Draw order per layer: X, W_gate, W_up, W_down, conv, W_target.
 * ``sweep``  as ``qwen`` with T=16384 per document and per-document X drawn
              from seed 1000+b; shared weights from seed 0.
 * ``stack``  L layers of ``qwen``-shaped weights (seed 0, layer-ordered draws),
-             h0 ~ N(0,1) (drawn after all layers), T=65536.
+             h0 ~ N(0,1) (drawn after all layers), T=65536.  At the full 36-layer
+             size the weights (2.9 G values) are drawn on the GPU instead
+             (``make_stack_device``: torch's device generator seeded with
+             seed*1000 + layer, draw order W_gate, W_up, W_down, conv,
+             W_target, then h0 from seed*1000 + L); those inputs never meet the
+             oracle, only properties that hold at any size.
 
 The same generators take smaller shapes for parity tests (``make_layer``).
 """
@@ -33,6 +38,7 @@ __all__ = [
     "make_tokens",
     "make_layer",
     "make_stack",
+    "make_stack_device",
     "CONFIGS",
 ]
 
@@ -129,6 +135,26 @@ def make_stack(n_layers: int, d: int, f: int, T: int, chunk: int, k: int, eta: f
     h0 = rng.standard_normal((T, d)).astype(np.float32)
     meta = dict(d=d, f=f, T=T, chunk=chunk, k=k, eta=float(eta), dtype=dtype)
     return h0, layers, meta
+
+
+def make_stack_device(n_layers: int, d: int, f: int, T: int, k: int, seed: int = 0,
+                      device="cuda", dtype=None):
+    """Full-size stack inputs drawn on the GPU: (h0 fp32 T x d, list of
+    per-layer weight dicts of `dtype` (default bf16) CUDA tensors)."""
+    import torch
+    dt = dtype or torch.bfloat16
+    layers = []
+    for li in range(n_layers):
+        g = torch.Generator(device=device).manual_seed(seed * 1000 + li)
+
+        def nrm(*shape):
+            return (torch.randn(*shape, generator=g, device=device) * 0.02).to(dt)
+
+        layers.append({"w_gate": nrm(f, d), "w_up": nrm(f, d), "w_down0": nrm(d, f),
+                       "conv_w": nrm(k, d), "w_target": nrm(d, d)})
+    g = torch.Generator(device=device).manual_seed(seed * 1000 + n_layers)
+    h0 = torch.randn(T, d, generator=g, device=device)
+    return h0, layers
 
 
 # Named workloads (sizes of the five measured configurations).
