@@ -142,6 +142,39 @@ def test_bf16_tcgen05_parity(T, C, starts):
     _check_layer(cfg, TOL_BF16, ttt_tol=TOL_TTT_PART, expect_path="tcgen05")
 
 
+@pytest.mark.parametrize("d,f,T,C,k,starts", [
+    (320, 576, 700, 100, 5, (0,)),       # 3 row blocks of d (a pair with one tile out of range), ragged f
+    (384, 320, 1030, 256, 8, (0, 515)),  # ragged f tile, 8 taps, a document start mid-group
+    (256, 256, 513, 1, 3, (0,)),         # one-token chunks: no chunk has a target, W stays W_0
+    (512, 1024, 2300, 512, 2, (0, 2047)),
+])
+def test_bf16_tcgen05_ragged_pairs(d, f, T, C, k, starts):
+    cfg = make_layer(d, f, T, C, k, 0.5, dtype="bf16", seed=d + f + T, init="qwen",
+                     doc_starts=starts)
+    layer = _check_layer(cfg, TOL_BF16, ttt_tol=TOL_TTT_PART, expect_path="tcgen05")
+    if C == 1:
+        assert torch.equal(layer.get_fast_weight().cpu(),
+                           torch.from_numpy(np.float32(cfg["w_down0"])))
+
+
+def test_empty_call_and_token_limit():
+    from chunk_wise_weight_ttt_b300 import TTTError
+    cfg = _bf16_cfg(T=256, C=64)
+    layer, dt = _make_gpu_layer(cfg)
+    x = _dev(cfg["x"], dt)
+    empty = x[:0]
+    o = layer.forward(empty, doc_starts=())
+    assert o.shape == (0, cfg["d"])
+    assert np.array_equal(_host(layer.get_fast_weight()), np.float64(cfg["w_down0"]))
+    big = torch.zeros((cfg["T"] + 1, cfg["d"]), dtype=dt, device="cuda")
+    with pytest.raises(TTTError, match="EINVAL"):
+        layer.forward(big)                             # one token over max_tokens
+    o = layer.forward(x)                               # exactly max_tokens
+    o_ref, _ = _oracle(cfg)
+    assert _rel(_host(o), o_ref) < TOL_BF16
+    layer.check()
+
+
 def test_bf16_simt_path_parity():
     cfg = _bf16_cfg(T=500, C=64)
     _check_layer(cfg, TOL_BF16, ttt_tol=TOL_TTT_PART, force_simt=True, expect_path="simt")
