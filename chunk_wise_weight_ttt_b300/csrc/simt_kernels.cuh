@@ -21,6 +21,35 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 
 constexpr int kMaxSpans = 256;
 
+// 8 consecutive elements (16-byte aligned for bf16, 32-byte for fp32) as floats.
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 q = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(h[e]);
+    v[2 * e] = f.x;
+    v[2 * e + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
+  uint4 q;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+  *reinterpret_cast<uint4*>(p) = q;
+}
+__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
 // Token spans whose chunking is regular: span i covers [start[i], start[i] +
 // len[i]) and its chunks are [start + c*chunk, ...) clipped to the span end.
 struct SpanList {
@@ -32,7 +61,8 @@ struct SpanList {
 
 // U[t] = sum_{j<k} conv[j] (.) X0[t+1+j] with every term at or past the end of
 // t's chunk dropped (chunk-local, causal-shifted depthwise Conv1D).  One
-// thread per (token, 8 channels).  Tokens outside every span are untouched.
+// thread per (token, 8 channels), vector loads and stores (rows are 16-byte
+// aligned: d is a multiple of 8).  Tokens outside every span are untouched.
 template <typename TIn, typename TOut>
 __global__ void conv_target_kernel(const TIn* __restrict__ x0, const TIn* __restrict__ conv_w,
                                    TOut* __restrict__ u, int d, int k, const SpanList spans) {
@@ -59,12 +89,13 @@ __global__ void conv_target_kernel(const TIn* __restrict__ x0, const TIn* __rest
     if (src >= cend) break;
     const TIn* xr = x0 + (size_t)src * d + c0;
     const TIn* wr = conv_w + (size_t)j * d + c0;
+    float xv[8], wv[8];
+    load8(xr, xv);
+    load8(wr, wv);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = fmaf(to_f(wr[e]), to_f(xr[e]), acc[e]);
+    for (int e = 0; e < 8; ++e) acc[e] = fmaf(wv[e], xv[e], acc[e]);
   }
-  TOut* ur = u + (size_t)t * d + c0;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) ur[e] = from_f<TOut>(acc[e]);
+  store8(u + (size_t)t * d + c0, acc);
 }
 
 // C(m,n) = alpha * sum_k A(m,k) B(k,n) + beta * C(m,n), fp32 accumulation.

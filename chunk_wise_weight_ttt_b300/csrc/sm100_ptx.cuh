@@ -120,6 +120,18 @@ __device__ __forceinline__ void cluster_sync_all() {
                    : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Block until every grid this one depends on has completed and its memory is
+// visible (returns at once when the grid was launched without a dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next dependent grid on the stream to be scheduled (its CTAs still
+// wait in griddep_wait for this grid to complete).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -464,6 +464,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   cluster_sync_all();  // both CTAs' barriers and TMEM exist before any pair traffic
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The prologue above may overlap the previous kernel's tail (programmatic
+  // dependent launch); no global memory is touched before that kernel is done.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {

@@ -229,8 +229,19 @@ std::vector<Span> plan_groups(int64_t n, int C, int G, const int64_t* ds, int nd
 
 int cdiv_h(int a, int b) { return (a + b - 1) / b; }
 
+// Programmatic dependent launch of the tcgen05 kernels (on unless TTT_PDL=0).
+bool use_pdl() {
+  static const bool on = [] {
+    const char* v = std::getenv("TTT_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
 // Launch the tcgen05 engine as clusters of two CTAs: one persistent cluster
-// per co-resident CTA pair, at most one per tile pair.
+// per co-resident CTA pair, at most one per tile pair.  With programmatic
+// dependent launch the grid's prologue overlaps the previous kernel's tail;
+// the kernel waits for that kernel before it touches global memory.
 template <int MODE>
 cudaError_t launch_pairs(int max_pairs, const GemmArgs& a, int npairs, cudaStream_t st) {
   if (npairs <= 0) return cudaSuccess;
@@ -239,13 +250,15 @@ cudaError_t launch_pairs(int max_pairs, const GemmArgs& a, int npairs, cudaStrea
   lc.blockDim = dim3(kGemmThreads);
   lc.dynamicSmemBytes = kGemmSmemBytes;
   lc.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = use_pdl() ? 2 : 1;
   return cudaLaunchKernelEx(&lc, tc_gemm_kernel<MODE>, a);
 }
 
