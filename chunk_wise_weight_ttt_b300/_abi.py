@@ -15,13 +15,14 @@ TTT_OK, TTT_EINVAL, TTT_EUNSUPPORTED, TTT_ECUDA, TTT_ETIMEOUT, TTT_EFAULT_INJECT
 STATUS_NAMES = {0: "TTT_OK", 1: "TTT_EINVAL", 2: "TTT_EUNSUPPORTED", 3: "TTT_ECUDA",
                 4: "TTT_ETIMEOUT", 5: "TTT_EFAULT_INJECTED"}
 TTT_F32, TTT_BF16 = 0, 1
+TTT_TARGET_NEXT, TTT_TARGET_CURRENT, TTT_TARGET_CAUSAL = 0, 1, 2
 NOALLOC_SCRATCH_BYTES = 32 << 20  # TTT_NOALLOC_SCRATCH_BYTES in the header
 
 
 class Config(C.Structure):
     _fields_ = [("d", C.c_int32), ("f", C.c_int32), ("chunk", C.c_int32), ("conv_k", C.c_int32),
                 ("n_docs", C.c_int32), ("eta", C.c_float), ("act_dtype", C.c_int32),
-                ("max_tokens", C.c_int64)]
+                ("max_tokens", C.c_int64), ("target_mode", C.c_int32), ("clip_tau", C.c_float)]
 
 
 _vp = C.c_void_p

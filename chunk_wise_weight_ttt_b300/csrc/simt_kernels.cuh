@@ -59,13 +59,15 @@ struct SpanList {
   int len[kMaxSpans];
 };
 
-// U[t] = sum_{j<k} conv[j] (.) X0[t+1+j] with every term at or past the end of
-// t's chunk dropped (chunk-local, causal-shifted depthwise Conv1D).  One
+// U[t] = sum_{j<k} conv[j] (.) X0[t + off(j)] with every term outside t's
+// chunk dropped (chunk-local depthwise Conv1D); off(j) = 1 + j (next-token
+// window), j (current-token window) or 1 - j (causal window), by `mode`.  One
 // thread per (token, 8 channels), vector loads and stores (rows are 16-byte
 // aligned: d is a multiple of 8).  Tokens outside every span are untouched.
 template <typename TIn, typename TOut>
 __global__ void conv_target_kernel(const TIn* __restrict__ x0, const TIn* __restrict__ conv_w,
-                                   TOut* __restrict__ u, int d, int k, const SpanList spans) {
+                                   TOut* __restrict__ u, int d, int k, const SpanList spans,
+                                   int mode) {
   const int groups_per_row = d / 8;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int first = spans.start[0];
@@ -80,13 +82,16 @@ __global__ void conv_target_kernel(const TIn* __restrict__ x0, const TIn* __rest
     if (spans.start[mid] <= t) lo = mid; else hi = mid - 1;
   }
   const int s0 = spans.start[lo];
-  const int cend = min(s0 + ((t - s0) / spans.chunk + 1) * spans.chunk, s0 + spans.len[lo]);
+  const int cbeg = s0 + ((t - s0) / spans.chunk) * spans.chunk;
+  const int cend = min(cbeg + spans.chunk, s0 + spans.len[lo]);
+  const int base = (mode == 1) ? 0 : 1;
+  const int step = (mode == 2) ? -1 : 1;
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
   for (int j = 0; j < k; ++j) {
-    const int src = t + 1 + j;
-    if (src >= cend) break;
+    const int src = t + base + step * j;
+    if (src < cbeg || src >= cend) continue;
     const TIn* xr = x0 + (size_t)src * d + c0;
     const TIn* wr = conv_w + (size_t)j * d + c0;
     float xv[8], wv[8];
@@ -205,6 +210,55 @@ __global__ void __launch_bounds__(256) simt_swiglu_kernel(int M, int N, int K, c
       Z[(long long)m * N + n] = (g / (1.0f + expf(-g))) * au[i][j];
     }
   }
+}
+
+constexpr int kMaxClipGroups = 256;
+
+// Groups of chunks whose same-chunk Gram blocks sit in `pitch` x `pitch` fp32
+// blocks (one per group, in order): group i covers tokens [start[i],
+// start[i] + len[i]) in chunks of `chunk` (the last may be short), at most G
+// chunks per group.
+struct GroupList {
+  int n, chunk, G, pitch;
+  int start[kMaxClipGroups];
+  int len[kMaxClipGroups];
+};
+
+// Per-chunk update clipping: one 256-thread block per chunk computes
+// ||V_c^T Z_c||_F^2 = sum_{i,j in c} (Z Z^T)_{ij} (V V^T)_{ij} from the Gram
+// blocks (fp64 accumulation in a fixed order), and when the norm exceeds tau
+// scales the chunk's rows of V (the eta-scaled target) by tau / norm, which
+// scales the chunk's delta V_c^T Z_c by the same factor.
+template <typename TV>
+__global__ void __launch_bounds__(256) clip_scale_kernel(const float* __restrict__ gz,
+                                                         const float* __restrict__ gv, TV* v,
+                                                         int d, float tau, const GroupList gl) {
+  const int gi = blockIdx.x / gl.G, ci = blockIdx.x % gl.G;
+  if (gi >= gl.n) return;
+  const int r0 = ci * gl.chunk;
+  const int len = gl.len[gi];
+  if (r0 >= len) return;
+  const int n = min(gl.chunk, len - r0);
+  const size_t base = (size_t)gi * gl.pitch * gl.pitch;
+  double acc = 0.0;
+  for (long long idx = threadIdx.x; idx < (long long)n * n; idx += blockDim.x) {
+    const int i = r0 + (int)(idx / n), j = r0 + (int)(idx % n);
+    const size_t o = base + (size_t)i * gl.pitch + j;
+    acc += (double)gz[o] * (double)gv[o];
+  }
+  __shared__ double red[256];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  const double nrm = sqrt(fmax(red[0], 0.0));
+  if (!(nrm > (double)tau)) return;
+  const float scale = (float)((double)tau / nrm);
+  TV* vr = v + (size_t)(gl.start[gi] + r0) * d;
+  for (long long e = threadIdx.x; e < (long long)n * d; e += blockDim.x)
+    vr[e] = from_f<TV>(to_f(vr[e]) * scale);
 }
 
 // dst[i] = float(src[i])  (fast-weight reset W <- W_0)

@@ -28,6 +28,9 @@
 //   kVProj   V = eta * (U W_target) with U the chunk-local Conv1D output.
 //   kSGram   per group of chunks, S = Z_g Z_g^T with every entry whose column
 //            chunk is not strictly before its row chunk set to zero.
+//   kDGram   per group of chunks, the same-chunk (block-diagonal) entries of
+//            M_g M_g^T in fp32 for M = Z or M = V (K = the matrix's width);
+//            the update-clipping norms come from these blocks.
 //   kGroup   one group of G chunks: the apply tiles
 //              O_g = Z_g W_s^T + S_g V_g            (W_s = state at group start)
 //            and the update tiles
@@ -75,12 +78,13 @@ constexpr int kWPreBlocks = (kWBoxes + kWBoxesPerStage - 1) / kWBoxesPerStage;
 constexpr int kStgBytesPerWarp = 32 * 128;
 constexpr int kEpiWarps = 4;
 
-enum GemmMode : int { kSwiGLU = 0, kVProj = 1, kSGram = 2, kGroup = 3 };
+enum GemmMode : int { kSwiGLU = 0, kVProj = 1, kSGram = 2, kGroup = 3, kDGram = 4 };
 
 // Tensor-map slots per mode (B boxes are the half that one CTA of a pair holds).
 //   kSwiGLU: 0 X (box 64x128), 1 Wg (64x128), 2 Wu (64x128)
 //   kVProj:  0 U (64x128), 1 W_target^T (64x128)
 //   kSGram:  0 Z (64x128), 1 Z (64x128)
+//   kDGram:  0 Z or V (64x128), 1 the same (64x128); `f` holds its width
 //   kGroup:  0 Z (64x128), 1 W_s bf16 (64x128), 2 S (64x128),
 //            3 V MN-major (64x64), 4 V MN-major with the group's K extent,
 //            5 Z MN-major (64x64) with the group's K extent,
@@ -130,7 +134,8 @@ template <int MODE>
 __device__ __forceinline__ int num_tiles(const GemmArgs& a) {
   if (MODE == kSwiGLU) return cdiv(cdiv(a.n_rows, kBM), 2) * cdiv(a.f, kBM);
   if (MODE == kVProj) return cdiv(cdiv(a.n_rows, kBM), 2) * cdiv(a.d, kBN);
-  if (MODE == kSGram) return a.n_groups * cdiv(cdiv(a.s_pad, kBM), 2) * cdiv(a.s_pad, kBN);
+  if (MODE == kSGram || MODE == kDGram)
+    return a.n_groups * cdiv(cdiv(a.s_pad, kBM), 2) * cdiv(a.s_pad, kBN);
   return cdiv(cdiv(a.glen, kBM), 2) * cdiv(a.d, kBN) + cdiv(cdiv(a.d, kBM), 2) * cdiv(a.f, kBN);
 }
 
@@ -170,6 +175,20 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int ra
     // the pair is computed if either tile is needed; the epilogue's mask makes
     // the extra entries zero
     ti.valid = (2 * mp * kBM < len) && (ti.n0 < corr_kbound(len, 2 * mp + 1, a.chunk));
+    ti.nkb1 = cdiv(a.f, kBK);
+  } else if (MODE == kDGram) {
+    const int mpt = cdiv(cdiv(a.s_pad, kBM), 2), nt = cdiv(a.s_pad, kBN);
+    const int g = t / (mpt * nt), r = t % (mpt * nt);
+    const int mp = r / nt, n = r % nt;
+    const int len = a.g_len[g];
+    ti.g = g;
+    ti.m0 = (2 * mp + rank) * kBM;
+    ti.n0 = n * kBN;
+    // computed when the pair's rows and the tile's columns share a chunk
+    const int r0 = 2 * mp * kBM, r1 = min(r0 + 2 * kBM, len) - 1;
+    const int c0 = ti.n0, c1 = min(c0 + kBN, len) - 1;
+    ti.valid = (r0 < len) && (c0 < len) && (r0 / a.chunk <= c1 / a.chunk) &&
+               (c0 / a.chunk <= r1 / a.chunk);
     ti.nkb1 = cdiv(a.f, kBK);
   } else {
     const int ntA = cdiv(a.d, kBN);
@@ -228,7 +247,7 @@ __device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& t
   } else if (MODE == kVProj) {
     tma_load_2d_pair(sa, &a.map[0], bar, kb * kBK, ti.m0);
     tma_load_2d_pair(sb, &a.map[1], bar, kb * kBK, ti.n0 + rank * kh);
-  } else if (MODE == kSGram) {
+  } else if (MODE == kSGram || MODE == kDGram) {
     const int gs = a.g_start[ti.g];
     tma_load_2d_pair(sa, &a.map[0], bar, kb * kBK, gs + ti.m0);
     tma_load_2d_pair(sb, &a.map[1], bar, kb * kBK, gs + ti.n0 + rank * kh);
@@ -375,6 +394,30 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
                              alpha * __uint_as_float(r[2 * j + 1]));
         const int col = ti.n0 + s * 32;
         if (ok) store_bf16x32(orow + col, p, a.d - col);
+      }
+    }
+  } else if (MODE == kDGram) {
+    // same-chunk entries of the Gram block in fp32, everything else 0
+    const int len = a.g_len[ti.g];
+    const int i = ti.m0 + row;
+    const int ci = i / a.chunk;
+    float* grow = reinterpret_cast<float*>(a.out0) + ((size_t)ti.g * a.s_pad + i) * a.s_pad;
+#pragma unroll 1
+    for (int s = 0; s < kBN / 32; ++s) {
+      tmem_ld32(tacc + s * 32, r);
+      tmem_ld_wait(r);
+      const int j0 = ti.n0 + s * 32;
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const bool keep = (i < len) && (j0 + j < len) && ((j0 + j) / a.chunk == ci);
+        v[j] = keep ? __uint_as_float(r[j]) : 0.0f;
+      }
+      if (i < a.s_pad) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(grow + j0 + 4 * q) =
+              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       }
     }
   } else {  // kSGram

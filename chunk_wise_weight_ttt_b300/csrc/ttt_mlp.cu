@@ -35,6 +35,7 @@ struct ttt_mlp {
   __nv_bfloat16* WtT;       // W_target transposed (out x in)
   void *Z, *U, *V;          // per-call intermediates (n x f, n x d, n x d)
   __nv_bfloat16* S;         // s_slots blocks of s_pad x s_pad
+  float *GZ, *GV;           // same-chunk Gram blocks for update clipping (or null)
   void *xs, *x0s, *os;      // host-staging copies of x, x0, o
   int* ctrl;                // [0] error word, [64..] tile counters
   int counter_next;
@@ -74,7 +75,7 @@ bool force_simt() {
 struct Layout {
   bool tc;
   int G, L, s_pad, s_slots;
-  size_t ctrl, W, Wb0, Wb1, WtT, Z, U, V, S, xs, x0s, os, total;
+  size_t ctrl, W, Wb0, Wb1, WtT, Z, U, V, S, GZ, GV, xs, x0s, os, total;
 };
 
 bool config_ok(const ttt_mlp_config* c, std::string* why) {
@@ -91,6 +92,9 @@ bool config_ok(const ttt_mlp_config* c, std::string* why) {
   if (c->act_dtype != TTT_F32 && c->act_dtype != TTT_BF16) return bad("act_dtype must be TTT_F32 or TTT_BF16");
   if (c->max_tokens < 1 || c->max_tokens > (int64_t(1) << 24)) return bad("max_tokens must be in 1..2^24");
   if (!std::isfinite(c->eta)) return bad("eta must be finite");
+  if (c->target_mode < TTT_TARGET_NEXT || c->target_mode > TTT_TARGET_CAUSAL)
+    return bad("target_mode must be TTT_TARGET_NEXT, TTT_TARGET_CURRENT or TTT_TARGET_CAUSAL");
+  if (!std::isfinite(c->clip_tau) || c->clip_tau < 0.0f) return bad("clip_tau must be 0 (off) or a positive finite number");
   return true;
 }
 
@@ -123,6 +127,13 @@ Layout make_layout(const ttt_mlp_config& c, bool tc) {
   l.U = take(n * d * inter);
   l.V = take(n * d * inter);
   l.S = tc ? take((size_t)l.s_slots * l.s_pad * l.s_pad * 2) : 0;
+  // same-chunk Gram blocks of Z and V for update clipping (fp32): per group
+  // of a wave on the tcgen05 path, one chunk at a time on the fp32 path
+  const size_t gram = c.clip_tau > 0.0f
+                          ? (tc ? (size_t)l.s_slots * l.s_pad * l.s_pad : (size_t)c.chunk * c.chunk) * 4
+                          : 0;
+  l.GZ = gram ? take(gram) : 0;
+  l.GV = gram ? take(gram) : 0;
   l.xs = take(n * d * act);
   l.x0s = take(n * d * act);
   l.os = take(n * d * act);
@@ -270,8 +281,9 @@ cudaError_t launch_gemm(ttt_mlp* h, GemmArgs& a, int npairs, cudaStream_t st) {
 // Kernel attributes of the tcgen05 engine and the number of CTA pairs that can
 // be resident at once (0 on failure).
 cudaError_t setup_tc_kernels(int* max_pairs) {
-  const void* kfn[4] = {(const void*)tc_gemm_kernel<kSwiGLU>, (const void*)tc_gemm_kernel<kVProj>,
-                        (const void*)tc_gemm_kernel<kSGram>, (const void*)tc_gemm_kernel<kGroup>};
+  const void* kfn[5] = {(const void*)tc_gemm_kernel<kSwiGLU>, (const void*)tc_gemm_kernel<kVProj>,
+                        (const void*)tc_gemm_kernel<kSGram>, (const void*)tc_gemm_kernel<kGroup>,
+                        (const void*)tc_gemm_kernel<kDGram>};
   for (const void* k : kfn) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
     if (e != cudaSuccess) return e;
@@ -329,8 +341,9 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
   const ttt_mlp_config& c = h->cfg;
   const int d = c.d, f = c.f;
   std::string why;
-  CUtensorMap map_x, map_u, map_za, map_zb, map_vmn, map_zmn;
+  CUtensorMap map_x, map_u, map_za, map_zb, map_vmn, map_zmn, map_va;
   if (!make_map(&map_x, x, d, n, d, 64, 128, &why) ||
+      !make_map(&map_va, h->V, d, n, d, 64, 128, &why) ||
       !make_map(&map_u, h->U, d, n, d, 64, 128, &why) ||
       !make_map(&map_za, h->Z, f, n, f, 64, 128, &why) ||
       !make_map(&map_zb, h->Z, f, n, f, 64, 128, &why) ||
@@ -357,7 +370,8 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
     }
     const long long cnt = (long long)(groups[w1 - 1].start + groups[w1 - 1].len - groups[w0].start) * (d / 8);
     conv_target_kernel<__nv_bfloat16, __nv_bfloat16><<<grid_for(cnt, 256), 256, 0, st>>>(
-        (const __nv_bfloat16*)x0, (const __nv_bfloat16*)h->conv, (__nv_bfloat16*)h->U, d, c.conv_k, sl);
+        (const __nv_bfloat16*)x0, (const __nv_bfloat16*)h->conv, (__nv_bfloat16*)h->U, d, c.conv_k, sl,
+        c.target_mode);
     TTT_CK_LAUNCH(h);
     h->prof_launches++;
   }
@@ -419,6 +433,36 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
     s.out0 = h->S;
     s.counter = next_counter(h, st);
     const int per = cdiv_h(cdiv_h(h->s_pad, kBM), 2) * cdiv_h(h->s_pad, kBN);
+    if (c.clip_tau > 0.0f) {
+      // per-chunk update clipping: same-chunk Gram blocks of V and Z, then
+      // each chunk's rows of V scaled by min(1, tau / ||V_c^T Z_c||_F)
+      GemmArgs q = s;
+      q.map[0] = map_va;
+      q.map[1] = map_va;
+      q.f = d;
+      q.out0 = h->GV;
+      q.counter = next_counter(h, st);
+      TTT_CK(h, launch_gemm<kDGram>(h, q, s.n_groups * per, st));
+      q.map[0] = map_za;
+      q.map[1] = map_za;
+      q.f = f;
+      q.out0 = h->GZ;
+      q.counter = next_counter(h, st);
+      TTT_CK(h, launch_gemm<kDGram>(h, q, s.n_groups * per, st));
+      GroupList gl{};
+      gl.n = s.n_groups;
+      gl.chunk = c.chunk;
+      gl.G = h->G;
+      gl.pitch = h->s_pad;
+      for (int i = 0; i < s.n_groups; ++i) {
+        gl.start[i] = s.g_start[i];
+        gl.len[i] = s.g_len[i];
+      }
+      clip_scale_kernel<__nv_bfloat16><<<gl.n * gl.G, 256, 0, st>>>(h->GZ, h->GV, (__nv_bfloat16*)h->V, d,
+                                                                     c.clip_tau, gl);
+      TTT_CK_LAUNCH(h);
+      h->prof_launches += 3;
+    }
     if (h->G > 1) {
       pt.begin(3);
       TTT_CK(h, launch_gemm<kSGram>(h, s, s.n_groups * per, st));
@@ -508,7 +552,8 @@ ttt_status forward_simt_t(ttt_mlp* h, int doc, const void* xv, const void* x0v, 
       sl.len[i - w0] = spans[i].len;
     }
     const long long cnt = (long long)(spans[w1 - 1].start + spans[w1 - 1].len - spans[w0].start) * (d / 8);
-    conv_target_kernel<T, float><<<grid_for(cnt, 256), 256, 0, st>>>(x0, (const T*)h->conv, U, d, c.conv_k, sl);
+    conv_target_kernel<T, float><<<grid_for(cnt, 256), 256, 0, st>>>(x0, (const T*)h->conv, U, d, c.conv_k, sl,
+                                                                     c.target_mode);
     TTT_CK_LAUNCH(h);
     h->prof_launches++;
   }
@@ -527,6 +572,28 @@ ttt_status forward_simt_t(ttt_mlp* h, int doc, const void* xv, const void* x0v, 
     simt_gemm_kernel<float, float, T><<<ga, 256, 0, st>>>(s.len, d, f, Z + (size_t)s.start * f, f, 1, W, 1, f,
                                                           o + (size_t)s.start * d, d, 1.0f, 0.0f);
     TTT_CK_LAUNCH(h);
+    if (c.clip_tau > 0.0f) {
+      // per-chunk update clipping (Gram form of ||V_c^T Z_c||_F, then V_c scaled)
+      dim3 gg((s.len + 63) / 64, (s.len + 63) / 64);
+      simt_gemm_kernel<float, float, float><<<gg, 256, 0, st>>>(s.len, s.len, f, Z + (size_t)s.start * f, f, 1,
+                                                                Z + (size_t)s.start * f, 1, f, h->GZ, c.chunk,
+                                                                1.0f, 0.0f);
+      TTT_CK_LAUNCH(h);
+      simt_gemm_kernel<float, float, float><<<gg, 256, 0, st>>>(s.len, s.len, d, V + (size_t)s.start * d, d, 1,
+                                                                V + (size_t)s.start * d, 1, d, h->GV, c.chunk,
+                                                                1.0f, 0.0f);
+      TTT_CK_LAUNCH(h);
+      GroupList gl{};
+      gl.n = 1;
+      gl.chunk = c.chunk;
+      gl.G = 1;
+      gl.pitch = c.chunk;
+      gl.start[0] = s.start;
+      gl.len[0] = s.len;
+      clip_scale_kernel<float><<<1, 256, 0, st>>>(h->GZ, h->GV, V, d, c.clip_tau, gl);
+      TTT_CK_LAUNCH(h);
+      h->prof_launches += 3;
+    }
     // update: W += (eta V_c)^T Z_c
     dim3 gu((f + 63) / 64, (d + 63) / 64);
     simt_gemm_kernel<float, float, float><<<gu, 256, 0, st>>>(d, f, s.len, V + (size_t)s.start * d, 1, d,
@@ -647,6 +714,8 @@ ttt_status ttt_mlp_create(const ttt_mlp_config* cfg, const void* w_gate, const v
   h->U = h->ws + l.U;
   h->V = h->ws + l.V;
   h->S = (__nv_bfloat16*)(h->ws + l.S);
+  h->GZ = l.GZ ? (float*)(h->ws + l.GZ) : nullptr;
+  h->GV = l.GV ? (float*)(h->ws + l.GV) : nullptr;
   h->xs = h->ws + l.xs;
   h->x0s = h->ws + l.x0s;
   h->os = h->ws + l.os;
@@ -956,7 +1025,7 @@ extern "C" ttt_status ttt_target_noalloc(const void* x0, const void* conv_w, con
     }
     const long long cnt = (long long)(docs[w1 - 1].start + docs[w1 - 1].len - docs[w0].start) * (d / 8);
     conv_target_kernel<__nv_bfloat16, __nv_bfloat16><<<grid_for(cnt, 256), 256, 0, st>>>(
-        (const __nv_bfloat16*)x0, (const __nv_bfloat16*)conv_w, u, d, conv_k, sl);
+        (const __nv_bfloat16*)x0, (const __nv_bfloat16*)conv_w, u, d, conv_k, sl, /*mode=*/0);
     TTT_CK(nullptr, cudaGetLastError());
   }
 

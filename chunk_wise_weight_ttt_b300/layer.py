@@ -49,7 +49,8 @@ class TTTMLP:
     """
 
     def __init__(self, w_gate, w_up, w_down0, conv_w, w_target, *, chunk: int, eta: float,
-                 n_docs: int = 1, max_tokens: int, stream=None, workspace=None):
+                 n_docs: int = 1, max_tokens: int, stream=None, workspace=None,
+                 target_mode: int = _abi.TTT_TARGET_NEXT, clip_tau: float = 0.0):
         self.lib = _abi.load()
         dt = w_gate.dtype
         if dt not in _DT:
@@ -61,7 +62,8 @@ class TTTMLP:
         self.d, self.f, self.k = d, f, conv_w.shape[0]
         self.dtype = dt
         self.cfg = Config(d=d, f=f, chunk=chunk, conv_k=self.k, n_docs=n_docs, eta=eta,
-                          act_dtype=_DT[dt], max_tokens=max_tokens)
+                          act_dtype=_DT[dt], max_tokens=max_tokens, target_mode=target_mode,
+                          clip_tau=clip_tau or 0.0)
         nbytes = self.lib.ttt_mlp_workspace_bytes(C.byref(self.cfg))
         if nbytes == 0:
             raise TTTError(_abi.TTT_EINVAL, "invalid configuration")
@@ -168,11 +170,12 @@ class TTTMLP:
 
 
 def workspace_bytes(d: int, f: int, *, chunk: int, conv_k: int, dtype=torch.bfloat16,
-                    n_docs: int = 1, max_tokens: int, eta: float = 0.0) -> int:
+                    n_docs: int = 1, max_tokens: int, eta: float = 0.0,
+                    target_mode: int = _abi.TTT_TARGET_NEXT, clip_tau: float = 0.0) -> int:
     """Device workspace (bytes) a layer of this shape needs."""
     lib = _abi.load()
     cfg = Config(d=d, f=f, chunk=chunk, conv_k=conv_k, n_docs=n_docs, eta=eta, act_dtype=_DT[dtype],
-                 max_tokens=max_tokens)
+                 max_tokens=max_tokens, target_mode=target_mode, clip_tau=clip_tau or 0.0)
     return int(lib.ttt_mlp_workspace_bytes(C.byref(cfg)))
 
 
@@ -191,15 +194,18 @@ class TTTStack:
     weights' dtype.
     """
 
-    def __init__(self, layers, *, chunk: int, eta: float, max_tokens: int, eps: float = 1e-6):
+    def __init__(self, layers, *, chunk: int, eta: float, max_tokens: int, eps: float = 1e-6,
+                 target_mode: int = _abi.TTT_TARGET_NEXT, clip_tau: float = 0.0):
         self.layers = layers
         w = layers[0]
         self.dtype = w["w_gate"].dtype
         f, d = w["w_gate"].shape
         self.d, self.f, self.k = d, f, w["conv_w"].shape[0]
         self.chunk, self.eta, self.max_tokens, self.eps = chunk, eta, max_tokens, eps
+        self.target_mode, self.clip_tau = target_mode, clip_tau
         nbytes = workspace_bytes(d, f, chunk=chunk, conv_k=self.k, dtype=self.dtype,
-                                 max_tokens=max_tokens, eta=eta)
+                                 max_tokens=max_tokens, eta=eta, target_mode=target_mode,
+                                 clip_tau=clip_tau)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=w["w_gate"].device)
 
     def forward(self, h0: torch.Tensor, doc_starts: Sequence[int] = (0,), stream=None,
@@ -216,7 +222,8 @@ class TTTStack:
             rmsnorm(h, x, self.eps, stream=stream)
             layer = TTTMLP(w["w_gate"], w["w_up"], w["w_down0"], w["conv_w"], w["w_target"],
                            chunk=self.chunk, eta=self.eta, max_tokens=self.max_tokens,
-                           stream=stream, workspace=self.workspace)
+                           stream=stream, workspace=self.workspace, target_mode=self.target_mode,
+                           clip_tau=self.clip_tau)
             layer.forward(x, x0, doc_starts=doc_starts, out=o, stream=stream)
             layer.check(stream=stream)
             layer.close()

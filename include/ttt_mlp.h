@@ -16,6 +16,12 @@
  *     W_{c+1} = W_c + eta V_c^T Z_c                            update
  *   The fast weight W (= the MLP's down projection) starts at the frozen
  *   W_down = W_0 and is reset to W_0 at every document start.
+ *   Options (ttt_mlp_config): the target window (target_mode, the ablation
+ *   axes and reconstruction target of section 4 / section 2 of the summary
+ *   page) and per-chunk update clipping (clip_tau: each chunk's delta
+ *   eta V_c^T Z_c is scaled by min(1, clip_tau / ||eta V_c^T Z_c||_F); the
+ *   summary page's appendix C.2 and section 6 of the walkthrough bound the
+ *   update delta's Frobenius norm).
  *
  * Conventions shared by every call:
  *   - Layouts are row-major.  W_gate, W_up: f x d; W_down (W_0): d x f;
@@ -61,6 +67,14 @@ typedef enum {
 
 typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
 
+/* Target window of U[t] = sum_{j<k} conv[j] (.) X0[t + off(j)]; every term
+ * whose token lies outside t's chunk is zero. */
+typedef enum {
+  TTT_TARGET_NEXT = 0,     /* off(j) = 1 + j: next token onwards (default) */
+  TTT_TARGET_CURRENT = 1,  /* off(j) = j: current token onwards (k = 1: reconstruction target) */
+  TTT_TARGET_CAUSAL = 2    /* off(j) = 1 - j: causal window ending at the next token */
+} ttt_target_mode;
+
 typedef struct {
   int32_t d;            /* model width; >= 8 and a multiple of 8 */
   int32_t f;            /* MLP intermediate width; >= 8 and a multiple of 8 */
@@ -70,6 +84,8 @@ typedef struct {
   float eta;            /* fast-weight learning rate */
   int32_t act_dtype;    /* ttt_dtype of X, X0, O and all weights */
   int64_t max_tokens;   /* largest n_tokens of one forward call; >= 1 */
+  int32_t target_mode;  /* ttt_target_mode */
+  float clip_tau;       /* per-chunk update clipping threshold; 0 = off, else > 0 */
 } ttt_mlp_config;
 
 typedef struct ttt_mlp ttt_mlp; /* opaque handle */
@@ -135,7 +151,8 @@ ttt_status ttt_mlp_destroy(ttt_mlp* h);
 const char* ttt_mlp_last_error(const ttt_mlp* h);
 
 /* Device pointers, inside the workspace, of the last forward call's Z
- * (n x f) and eta-scaled target V (n x d, i.e. eta * U W_target), and their
+ * (n x f) and eta-scaled target V (n x d, i.e. eta * U W_target, times each
+ * chunk's clip scale when clipping is on), and their
  * element type (*dtype: TTT_BF16 on the tcgen05 path, TTT_F32 on the SIMT
  * path).  For inspection and tests; valid until the next forward call. */
 ttt_status ttt_mlp_intermediates(const ttt_mlp* h, const void** z, const void** v,
@@ -165,7 +182,8 @@ const char* ttt_mlp_path(const ttt_mlp* h);
  * cudaMalloc is forbidden or unavailable) and so cannot provide the
  * workspace the handle-based calls need.
  *
- * It computes the same target as a forward call, V = eta * Conv1D(X0) W_target
+ * It computes the same target as a forward call with the default window
+ * (TTT_TARGET_NEXT) and no clipping, V = eta * Conv1D(X0) W_target
  * (chunk-local, causal-shifted depthwise Conv1D; chunking restarts at each
  * document start), into the caller's v, with the bf16 tensor-core kernels.
  * Its scratch (the Conv1D output, the transposed W_target, a tile counter and

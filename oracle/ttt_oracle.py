@@ -28,7 +28,15 @@ design notes):
   R3  The update is W <- W + eta * V^T Z with no 1/C factor ([BLOG] 2 and 4).
   R4  Chunking restarts at every document start; a document's last chunk may
       be shorter than C.  A call's trailing partial chunk is a short chunk.
-  R5  Update clipping ([SUM] C.2) is off on this path.
+  R5  Update clipping ([SUM] C.2; [BLOG] 6) is optional and per chunk: when a
+      threshold tau is given, the chunk's delta eta V^T Z is scaled by
+      min(1, tau / ||eta V^T Z||_F) before it is added (the pages bound "the
+      Frobenius norm of the update delta"; one delta per chunk).
+  R6  Target variants (ablation axes of [SUM] 4 and the reconstruction target
+      of [SUM] 2 / [BLOG] 4) are windows at other offsets, cut at the chunk
+      edges like R1: mode 1 starts at the current token (k = 1 is the
+      reconstruction target X0[t]); mode 2 is a causal window that ends at the
+      next token.
 
 Function-level parity status: every public function here is pinned by a
 "not gpu" test (brute force, closed forms, library routines, invariants).
@@ -38,16 +46,37 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
+    "TARGET_NEXT",
+    "TARGET_CURRENT",
+    "TARGET_CAUSAL",
     "silu",
     "swiglu_intermediate",
     "chunk_target_source",
     "chunk_target",
+    "clip_delta",
+    "chunk_delta_norms",
     "chunk_spans",
     "ttt_layer",
     "ttt_layer_rows",
     "rms_norm",
     "ttt_stack",
 ]
+
+
+# Target windows (reading R1 and R6): offset of tap j from token t.
+TARGET_NEXT = 0     # X0[t+1+j]
+TARGET_CURRENT = 1  # X0[t+j]
+TARGET_CAUSAL = 2   # X0[t+1-j]
+
+
+def _tap_offset(mode: int, j: int) -> int:
+    if mode == TARGET_NEXT:
+        return 1 + j
+    if mode == TARGET_CURRENT:
+        return j
+    if mode == TARGET_CAUSAL:
+        return 1 - j
+    raise ValueError(f"unknown target mode {mode}")
 
 
 def _f64(a) -> np.ndarray:
@@ -72,28 +101,40 @@ def swiglu_intermediate(x, w_gate, w_up) -> np.ndarray:
     return silu(x @ _f64(w_gate).T) * (x @ _f64(w_up).T)
 
 
-def chunk_target_source(x0_chunk, conv_w) -> np.ndarray:
+def chunk_target_source(x0_chunk, conv_w, mode: int = TARGET_NEXT) -> np.ndarray:
     """Depthwise causal-shifted Conv1D of one chunk's embeddings (reading R1).
 
     U[t] = sum_{j=0}^{k-1} conv[j] (elementwise) X0[t+1+j], terms whose token
     index t+1+j reaches the chunk's end are zero, so no information enters
-    from another chunk ([BLOG] 6; "causal padding", [SUM] B).
+    from another chunk ([BLOG] 6; "causal padding", [SUM] B).  Other windows
+    (reading R6): mode TARGET_CURRENT uses X0[t+j], TARGET_CAUSAL X0[t+1-j];
+    every term whose token lies outside the chunk is zero.
     x0_chunk: n x d, conv_w: k x d -> n x d."""
     x0 = _f64(x0_chunk)
     cw = _f64(conv_w)
     n, d = x0.shape
     u = np.zeros((n, d), dtype=np.float64)
     for j in range(cw.shape[0]):
-        m = n - (1 + j)  # tokens t with t+1+j < n
-        if m > 0:
-            u[:m] += cw[j][None, :] * x0[1 + j:1 + j + m]
+        o = _tap_offset(mode, j)
+        t0, t1 = max(0, -o), min(n, n - o)  # tokens t with 0 <= t+o < n
+        if t1 > t0:
+            u[t0:t1] += cw[j][None, :] * x0[t0 + o:t1 + o]
     return u
 
 
-def chunk_target(x0_chunk, conv_w, w_target) -> np.ndarray:
+def chunk_target(x0_chunk, conv_w, w_target, mode: int = TARGET_NEXT) -> np.ndarray:
     """LM-aligned target V = Conv1D(X0) W_target ([SUM] 3 LM-Aligned Objective;
     [BLOG] 4).  w_target: d x d, given as in x out."""
-    return chunk_target_source(x0_chunk, conv_w) @ _f64(w_target)
+    return chunk_target_source(x0_chunk, conv_w, mode) @ _f64(w_target)
+
+
+def clip_delta(delta, clip_tau):
+    """Per-chunk update clipping (reading R5): delta * min(1, tau/||delta||_F);
+    no clipping when clip_tau is None or 0."""
+    if not clip_tau:
+        return delta
+    nrm = float(np.linalg.norm(delta))
+    return delta * (clip_tau / nrm) if nrm > clip_tau else delta
 
 
 def chunk_spans(n_tokens: int, chunk: int, doc_starts=(0,)):
@@ -121,7 +162,7 @@ def chunk_spans(n_tokens: int, chunk: int, doc_starts=(0,)):
 
 
 def ttt_layer(x, x0, w_gate, w_up, w_down0, conv_w, w_target, eta, chunk,
-              doc_starts=(0,), w_init=None):
+              doc_starts=(0,), w_init=None, target_mode=TARGET_NEXT, clip_tau=None):
     """One TTT-MLP layer over one call's tokens, the sequential recursion.
 
     For every chunk c in order ([BLOG] 3 "apply then update"):
@@ -130,7 +171,9 @@ def ttt_layer(x, x0, w_gate, w_up, w_down0, conv_w, w_target, eta, chunk,
       V_c = Conv1D(X0_c) W_target          (chunk-local target)
       W_{c+1} = W_c + eta V_c^T Z_c        ([BLOG] 2, 4)
     W starts at ``w_init`` (default W_0 = w_down0) and is reset to W_0 at each
-    document start ([SUM] B).  Returns (O n x d, final W d x f), float64."""
+    document start ([SUM] B).  ``target_mode`` picks the target window (R1,
+    R6); ``clip_tau`` clips each chunk's delta (R5).  Returns (O n x d, final
+    W d x f), float64."""
     x = _f64(x)
     x0 = _f64(x0)
     w0 = _f64(w_down0)
@@ -142,20 +185,23 @@ def ttt_layer(x, x0, w_gate, w_up, w_down0, conv_w, w_target, eta, chunk,
             W = w0.copy()
         z = swiglu_intermediate(x[s:e], w_gate, w_up)
         out[s:e] = z @ W.T
-        v = chunk_target(x0[s:e], conv_w, w_target)
-        W = W + float(eta) * (v.T @ z)
+        v = chunk_target(x0[s:e], conv_w, w_target, target_mode)
+        W = W + clip_delta(float(eta) * (v.T @ z), clip_tau)
     return out, W
 
 
 def ttt_layer_rows(x, x0, w_gate, w_up, w_down0, conv_w, w_target, eta, chunk,
-                   rows, doc_starts=(0,), w_init=None, z=None):
+                   rows, doc_starts=(0,), w_init=None, z=None, target_mode=TARGET_NEXT,
+                   clip_tau=None):
     """The same recursion restricted to a subset of W's rows.
 
     Row i of W, and column i of O, depend on all of Z but only on column i of
     V (W[i] += eta * sum_t V[t,i] Z[t]; O[t,i] = Z[t] . W[i]).  So the sampled
     rows are exact without computing the others.  ``z`` may pass in
     swiglu_intermediate(x, w_gate, w_up) when several runs share the tokens (Z
-    does not depend on the chunking or on W).  Returns (O[:, rows], W[rows])."""
+    does not depend on the chunking or on W).  With ``clip_tau`` the clip scale
+    of each chunk needs the whole delta's norm, which is computed in full.
+    Returns (O[:, rows], W[rows])."""
     rows = np.asarray(rows, dtype=np.int64)
     x = _f64(x)
     x0 = _f64(x0)
@@ -169,9 +215,28 @@ def ttt_layer_rows(x, x0, w_gate, w_up, w_down0, conv_w, w_target, eta, chunk,
             W = w0r.copy()
         zc = swiglu_intermediate(x[s:e], w_gate, w_up) if z is None else _f64(z[s:e])
         out[s:e] = zc @ W.T
-        v = chunk_target_source(x0[s:e], conv_w) @ wt
-        W = W + float(eta) * (v.T @ zc)
+        src = chunk_target_source(x0[s:e], conv_w, target_mode)
+        v = src @ wt
+        scale = 1.0
+        if clip_tau:
+            nrm = float(np.linalg.norm(float(eta) * ((src @ _f64(w_target)).T @ zc)))
+            scale = clip_tau / nrm if nrm > clip_tau else 1.0
+        W = W + scale * (float(eta) * (v.T @ zc))
     return out, W
+
+
+def chunk_delta_norms(x, x0, w_gate, w_up, conv_w, w_target, eta, chunk, doc_starts=(0,),
+                      target_mode=TARGET_NEXT, z=None):
+    """||eta V_c^T Z_c||_F of every chunk's unclipped delta, in chunk order
+    (the quantity the clipping of reading R5 compares with its threshold)."""
+    x = _f64(x)
+    x0 = _f64(x0)
+    out = []
+    for s, e, _ in chunk_spans(x.shape[0], chunk, doc_starts):
+        zc = swiglu_intermediate(x[s:e], w_gate, w_up) if z is None else _f64(z[s:e])
+        v = chunk_target(x0[s:e], conv_w, w_target, target_mode)
+        out.append(float(np.linalg.norm(float(eta) * (v.T @ zc))))
+    return np.array(out)
 
 
 def rms_norm(h, eps=1e-6) -> np.ndarray:
@@ -181,7 +246,7 @@ def rms_norm(h, eps=1e-6) -> np.ndarray:
 
 
 def ttt_stack(h0, layers, eta, chunk, doc_starts=(0,), eps=1e-6, n_layers=None,
-              x0=None):
+              x0=None, target_mode=TARGET_NEXT, clip_tau=None):
     """Stack of pre-norm residual SwiGLU+TTT MLP blocks (no attention).
 
     h_{l+1} = h_l + TTT_MLP_l(RMSNorm(h_l)) with X0 = h_0 for every layer
@@ -195,7 +260,8 @@ def ttt_stack(h0, layers, eta, chunk, doc_starts=(0,), eps=1e-6, n_layers=None,
     finals = []
     for li, w in enumerate(layers[: n_layers or len(layers)]):
         o, wf = ttt_layer(rms_norm(h, eps), x0, w["w_gate"], w["w_up"], w["w_down0"],
-                          w["conv_w"], w["w_target"], eta, chunk, doc_starts)
+                          w["conv_w"], w["w_target"], eta, chunk, doc_starts,
+                          target_mode=target_mode, clip_tau=clip_tau)
         h = h + o
         finals.append(wf)
     return h, finals

@@ -50,9 +50,17 @@ def test_workspace_bytes_valid_and_invalid(lib):
     assert good >= 64 * 256 * 4 + 1024 * (256 + 2 * 64) * 4
     for bad in [dict(d=0), dict(d=12), dict(f=7), dict(chunk=0), dict(chunk=1025),
                 dict(conv_k=0), dict(conv_k=9), dict(n_docs=0), dict(act_dtype=7),
-                dict(max_tokens=0), dict(eta=float("nan"))]:
+                dict(max_tokens=0), dict(eta=float("nan")), dict(target_mode=3),
+                dict(target_mode=-1), dict(clip_tau=-1.0), dict(clip_tau=float("inf"))]:
         assert lib.ttt_mlp_workspace_bytes(C.byref(_cfg(**bad))) == 0, bad
     assert lib.ttt_mlp_workspace_bytes(None) == 0
+
+
+def test_clipping_adds_gram_workspace(lib):
+    plain = lib.ttt_mlp_workspace_bytes(C.byref(_cfg()))
+    clip = lib.ttt_mlp_workspace_bytes(C.byref(_cfg(clip_tau=1e-5)))
+    assert clip >= plain + 2 * 64 * 64 * 4  # two fp32 same-chunk Gram blocks (fp32 path)
+    assert lib.ttt_mlp_workspace_bytes(C.byref(_cfg(target_mode=2))) == plain
 
 
 def test_workspace_bytes_qwen_layer(lib):

@@ -88,6 +88,52 @@ def test_conv_matches_torch_conv1d(k, n):
                                rtol=1e-13, atol=1e-13)
 
 
+def _torch_target_source_mode(x0_chunk, conv_w, mode):
+    """Library conv1d for the other windows: mode 1 (X0[t+j]) is conv1d on the
+    chunk zero-padded at its end; mode 2 (X0[t+1-j]) is conv1d with the taps
+    reversed over the chunk zero-padded on both sides (k zeros before, 2
+    after), read at output t+2."""
+    x0 = _t(x0_chunk)
+    n, d = x0.shape
+    k = conv_w.shape[0]
+    w = _t(conv_w)
+    if mode == 1:
+        seq = torch.cat([x0, torch.zeros((k, d), dtype=TORCH64)])
+        out = F.conv1d(seq.T.unsqueeze(0), w.T.unsqueeze(1), groups=d)
+        return out[0, :, :n].T.numpy()
+    seq = torch.cat([torch.zeros((k, d), dtype=TORCH64), x0, torch.zeros((2, d), dtype=TORCH64)])
+    out = F.conv1d(seq.T.unsqueeze(0), w.flip(0).T.unsqueeze(1), groups=d)
+    return out[0, :, 2:n + 2].T.numpy()
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("k", [1, 2, 5, 8])
+@pytest.mark.parametrize("n", [1, 3, 9])
+def test_target_modes_match_torch_conv1d(mode, k, n):
+    rng = np.random.default_rng(100 * mode + 10 * k + n)
+    x0 = rng.standard_normal((n, 5))
+    cw = rng.standard_normal((k, 5))
+    np.testing.assert_allclose(orc.chunk_target_source(x0, cw, mode),
+                               _torch_target_source_mode(x0, cw, mode), rtol=1e-13, atol=1e-13)
+
+
+def test_current_window_k1_is_reconstruction_target():
+    rng = np.random.default_rng(4)
+    x0 = rng.standard_normal((6, 3))
+    cw = rng.standard_normal((1, 3))
+    wt = rng.standard_normal((3, 3))
+    v = orc.chunk_target(x0, cw, wt, orc.TARGET_CURRENT)
+    np.testing.assert_allclose(v, (cw[0] * x0) @ wt, rtol=1e-14)
+
+
+def test_causal_and_next_windows_agree_for_one_tap():
+    rng = np.random.default_rng(5)
+    x0 = rng.standard_normal((7, 4))
+    cw = rng.standard_normal((1, 4))
+    np.testing.assert_array_equal(orc.chunk_target_source(x0, cw, orc.TARGET_CAUSAL),
+                                  orc.chunk_target_source(x0, cw, orc.TARGET_NEXT))
+
+
 def test_k1_is_next_token_target():
     rng = np.random.default_rng(0)
     x0 = rng.standard_normal((5, 3))
@@ -125,8 +171,10 @@ def _silu_scalar(a):
     return a / (1.0 + math.exp(-a))
 
 
-def brute_force_layer(x, x0, wg, wu, w0, cw, wt, eta, C, doc_starts=(0,)):
-    """Scalar, per-token restatement of the whole method (tiny shapes only)."""
+def brute_force_layer(x, x0, wg, wu, w0, cw, wt, eta, C, doc_starts=(0,), mode=0, tau=None):
+    """Scalar, per-token restatement of the whole method (tiny shapes only).
+    mode: target window (0: X0[t+1+j], 1: X0[t+j], 2: X0[t+1-j]); tau: clip
+    each chunk's delta to Frobenius norm tau."""
     x = np.asarray(x, np.float64).tolist()
     x0 = np.asarray(x0, np.float64).tolist()
     wg = np.asarray(wg, np.float64).tolist()
@@ -158,16 +206,22 @@ def brute_force_layer(x, x0, wg, wu, w0, cw, wt, eta, C, doc_starts=(0,)):
         for i in range(t, e):
             src = [0.0] * d
             for j in range(k):
-                if i + 1 + j < e:
+                s_tok = i + (1 + j, j, 1 - j)[mode]
+                if t <= s_tok < e:
                     for a in range(d):
-                        src[a] += cw[j][a] * x0[i + 1 + j][a]
+                        src[a] += cw[j][a] * x0[s_tok][a]
             for r in range(d):
                 v = sum(src[a] * wt[a][r] for a in range(d))
                 for p in range(f):
                     dW[r][p] += v * zs[i - t][p]
+        scale = eta
+        if tau:
+            nrm = math.sqrt(sum((eta * dW[r][p]) ** 2 for r in range(d) for p in range(f)))
+            if nrm > tau:
+                scale = eta * tau / nrm
         for r in range(d):
             for p in range(f):
-                W[r][p] += eta * dW[r][p]
+                W[r][p] += scale * dW[r][p]
         t = e
     return np.array(out), np.array(W)
 
@@ -189,6 +243,17 @@ def test_brute_force_tiny(case):
     ob, wb = brute_force_layer(cfg["x"], cfg["x0"], cfg["w_gate"], cfg["w_up"], cfg["w_down0"],
                                cfg["conv_w"], cfg["w_target"], cfg["eta"], cfg["chunk"],
                                cfg["doc_starts"])
+    assert _rel(o, ob) < 1e-12
+    assert _rel(w, wb) < 1e-12
+
+
+@pytest.mark.parametrize("mode,tau", [(1, None), (2, None), (0, 0.05), (2, 0.02), (1, 1e9)])
+def test_brute_force_target_modes_and_clipping(mode, tau):
+    cfg = _tiny(T=13, C=4, k=3, doc_starts=(0, 9), eta=0.8)
+    o, w = _run(cfg, target_mode=mode, clip_tau=tau)
+    ob, wb = brute_force_layer(cfg["x"], cfg["x0"], cfg["w_gate"], cfg["w_up"], cfg["w_down0"],
+                               cfg["conv_w"], cfg["w_target"], cfg["eta"], cfg["chunk"],
+                               cfg["doc_starts"], mode=mode, tau=tau)
     assert _rel(o, ob) < 1e-12
     assert _rel(w, wb) < 1e-12
 
@@ -261,6 +326,55 @@ def test_recurrence_equals_prefix_form(T, C):
         assert _rel(o, o0) > 1e-3
 
 
+def test_clipping_bounds_every_chunk_delta():
+    """With clipping, each chunk's delta keeps its direction and has norm
+    min(||unclipped||, tau); a huge tau changes nothing."""
+    cfg = _tiny(d=8, f=20, T=40, C=8, k=3, eta=0.9)
+    tau = 0.05
+    W = np.float64(cfg["w_down0"])
+    for s, e, _ in orc.chunk_spans(cfg["T"], cfg["chunk"], (0,)):
+        sub = {**cfg, "x": cfg["x"][s:e], "x0": cfg["x0"][s:e]}
+        _, w_free = _run(sub, doc_starts=(), w_init=W)
+        _, w_clip = _run(sub, doc_starts=(), w_init=W, clip_tau=tau)
+        d_free, d_clip = w_free - W, w_clip - W
+        n_free = np.linalg.norm(d_free)
+        assert np.linalg.norm(d_clip) <= min(n_free, tau) * (1 + 1e-12)
+        if n_free > tau:
+            assert abs(np.linalg.norm(d_clip) - tau) <= 1e-12 * tau
+            np.testing.assert_allclose(d_clip * n_free / tau, d_free, rtol=1e-10, atol=1e-14)
+        W = w_clip
+    o1, w1 = _run(cfg)
+    o2, w2 = _run(cfg, clip_tau=1e12)
+    assert np.array_equal(o1, o2) and np.array_equal(w1, w2)
+
+
+def test_chunk_delta_norms_are_the_recursions_deltas():
+    cfg = _tiny(d=8, f=20, T=30, C=7, k=3, doc_starts=(0, 16))
+    norms = orc.chunk_delta_norms(cfg["x"], cfg["x0"], cfg["w_gate"], cfg["w_up"], cfg["conv_w"],
+                                  cfg["w_target"], cfg["eta"], cfg["chunk"], cfg["doc_starts"])
+    spans = orc.chunk_spans(cfg["T"], cfg["chunk"], cfg["doc_starts"])
+    assert len(norms) == len(spans)
+    W = np.float64(cfg["w_down0"])
+    for (s, e, reset), nrm in zip(spans, norms):
+        if reset:
+            W = np.float64(cfg["w_down0"])
+        sub = {**cfg, "x": cfg["x"][s:e], "x0": cfg["x0"][s:e]}
+        _, w_next = _run(sub, doc_starts=(), w_init=W)
+        assert abs(np.linalg.norm(w_next - W) - nrm) <= 1e-12 * max(nrm, 1e-300)
+        W = w_next
+
+
+def test_gram_identity_for_the_update_norm():
+    """||V^T Z||_F^2 = <V V^T, Z Z^T>_F (the form the kernels use to get a
+    chunk's delta norm without forming the delta), checked with torch."""
+    rng = np.random.default_rng(9)
+    v = _t(rng.standard_normal((16, 7)))
+    z = _t(rng.standard_normal((16, 11)))
+    lhs = torch.linalg.matrix_norm(v.T @ z) ** 2
+    rhs = torch.sum((v @ v.T) * (z @ z.T))
+    assert abs(float(lhs - rhs)) <= 1e-12 * float(lhs)
+
+
 def test_affine_in_eta():
     cfg = _tiny(d=8, f=20, T=48, C=8, k=3)
     o0, w0 = _run(cfg, eta=0.0)
@@ -311,6 +425,15 @@ def test_row_sampled_equals_full():
                                       cfg["chunk"], rows, cfg["doc_starts"], z=z)
     assert _rel(orow2, o[:, rows]) < 1e-13
     assert _rel(wrow2, w[rows]) < 1e-13
+    # other target windows and clipping: rows still equal the full recursion
+    for mode, tau in ((2, 0.01), (1, None)):
+        o3, w3 = _run(cfg, target_mode=mode, clip_tau=tau)
+        orow3, wrow3 = orc.ttt_layer_rows(cfg["x"], cfg["x0"], cfg["w_gate"], cfg["w_up"],
+                                          cfg["w_down0"], cfg["conv_w"], cfg["w_target"],
+                                          cfg["eta"], cfg["chunk"], rows, cfg["doc_starts"],
+                                          target_mode=mode, clip_tau=tau)
+        assert _rel(orow3, o3[:, rows]) < 1e-13
+        assert _rel(wrow3, w3[rows]) < 1e-13
 
 
 def test_stack_matches_brute_force_composition():
@@ -349,6 +472,9 @@ def _pins_pass(module_overrides):
             lambda: test_recurrence_equals_prefix_form(50, 7),
             lambda: test_no_cross_chunk_target_leakage(),
             lambda: test_reset_matches_documents_run_alone(),
+            lambda: test_brute_force_target_modes_and_clipping(0, 0.05),
+            lambda: test_brute_force_target_modes_and_clipping(2, None),
+            lambda: test_target_modes_match_torch_conv1d(2, 5, 9),
         ]
         for c in checks:
             try:
@@ -379,7 +505,7 @@ def _no_reset_spans(n, chunk, doc_starts=(0,)):
     return [(s, e, s == 0) for s, e, _ in _ORIG_SPANS(n, chunk, doc_starts)]
 
 
-def _current_token_conv(x0_chunk, conv_w):
+def _current_token_conv(x0_chunk, conv_w, mode=0):
     x0 = np.float64(x0_chunk)
     u = np.zeros_like(x0)
     for j in range(conv_w.shape[0]):
@@ -389,7 +515,7 @@ def _current_token_conv(x0_chunk, conv_w):
     return u
 
 
-def _leaky_conv(x0_chunk, conv_w):
+def _leaky_conv(x0_chunk, conv_w, mode=0):
     # forgets the chunk-end padding: wraps around inside the chunk
     x0 = np.float64(x0_chunk)
     u = np.zeros_like(x0)
@@ -400,6 +526,19 @@ def _leaky_conv(x0_chunk, conv_w):
 
 _ORIG_SPANS = orc.chunk_spans
 _ORIG_TARGET = orc.chunk_target
+_ORIG_SOURCE = orc.chunk_target_source
+
+
+def _causal_off_by_one(x0_chunk, conv_w, mode=0):
+    # the causal window ending at the current token instead of the next one
+    return _ORIG_SOURCE(x0_chunk, conv_w, 1 if mode == 2 else mode) if mode != 2 else \
+        np.vstack([np.zeros((1, np.shape(x0_chunk)[1])),
+                   _ORIG_SOURCE(x0_chunk, conv_w, 2)[:-1]])
+
+
+def _clip_by_max(delta, tau):
+    m = float(np.max(np.abs(delta)))
+    return delta * (tau / m) if tau and m > tau else delta
 
 
 def test_planted_mistakes_are_caught():
@@ -409,10 +548,13 @@ def test_planted_mistakes_are_caught():
         "no document reset": {"chunk_spans": _no_reset_spans},
         "target from the current token": {"chunk_target_source": _current_token_conv},
         "target wraps inside the chunk": {"chunk_target_source": _leaky_conv},
-        "W_target transposed": {"chunk_target": lambda x0, cw, wt: orc.chunk_target_source(x0, cw)
-                                @ np.float64(wt).T},
-        "update sign flipped": {"chunk_target": lambda x0, cw, wt: -_ORIG_TARGET(x0, cw, wt)},
+        "W_target transposed": {"chunk_target": lambda x0, cw, wt, mode=0:
+                                orc.chunk_target_source(x0, cw) @ np.float64(wt).T},
+        "update sign flipped": {"chunk_target": lambda x0, cw, wt, mode=0: -_ORIG_TARGET(x0, cw, wt)},
         "SiLU sign flipped": {"silu": lambda a: np.float64(a) / (1 + np.exp(np.float64(a)))},
+        "clipping ignored": {"clip_delta": lambda delta, tau: delta},
+        "clipping by max-abs, not Frobenius": {"clip_delta": _clip_by_max},
+        "causal window shifted by one token": {"chunk_target_source": _causal_off_by_one},
     }
     for name, ov in mistakes.items():
         assert not _pins_pass(ov), f"planted mistake not caught: {name}"

@@ -85,6 +85,38 @@ def test_qwen_layer_full_size():
     assert part <= 5e-2
 
 
+def test_qwen_layer_clipping_and_causal_window_full_size():
+    """The same layer with the causal target window and per-chunk clipping at
+    the median chunk-delta norm (about half the chunks clipped)."""
+    c = CONFIGS["qwen"]
+    cfg = make_layer(c["d"], c["f"], c["T"], c["chunk"], c["k"], c["eta"], dtype="bf16", seed=0,
+                     init="qwen")
+    z = orc.swiglu_intermediate(cfg["x"], cfg["w_gate"], cfg["w_up"])
+    norms = orc.chunk_delta_norms(cfg["x"], cfg["x"], cfg["w_gate"], cfg["w_up"], cfg["conv_w"],
+                                  cfg["w_target"], cfg["eta"], cfg["chunk"], (0,),
+                                  target_mode=orc.TARGET_CAUSAL, z=z)
+    tau = float(np.median(norms))
+    from chunk_wise_weight_ttt_b300 import TTTMLP
+    ws = [_dev(cfg[k]) for k in ("w_gate", "w_up", "w_down0", "conv_w", "w_target")]
+    layer = TTTMLP(*ws, chunk=cfg["chunk"], eta=cfg["eta"], max_tokens=cfg["T"],
+                   target_mode=orc.TARGET_CAUSAL, clip_tau=tau)
+    o = layer.forward(_dev(cfg["x"]), doc_starts=(0,))
+    w = layer.get_fast_weight()
+    layer.check()
+    og, wg = _host(o), _host(w)
+    rows = _rows(c["d"], seed=99)
+    o_ref, w_ref = orc.ttt_layer_rows(cfg["x"], cfg["x"], cfg["w_gate"], cfg["w_up"],
+                                      cfg["w_down0"], cfg["conv_w"], cfg["w_target"], cfg["eta"],
+                                      cfg["chunk"], rows, (0,), z=z,
+                                      target_mode=orc.TARGET_CAUSAL, clip_tau=tau)
+    eo, ew = _rel(og[:, rows], o_ref), _rel(wg[rows], w_ref)
+    w0 = np.float64(cfg["w_down0"])[rows]
+    edw = _rel(wg[rows] - w0, w_ref - w0)
+    print(f"causal window + clipping (tau {tau:.3e}): O err {eo:.3e}  W err {ew:.3e}  "
+          f"W-W0 err {edw:.3e}")
+    assert eo <= TOL and ew <= TOL and edw <= 5e-2
+
+
 def test_long_context_with_resets_full_size():
     """T=131072 with documents starting every 32768 tokens: sampled rows match
     the oracle, and every document's output equals that document run alone
