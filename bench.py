@@ -112,6 +112,14 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def group_tokens() -> int:
+    """Tokens per fused apply+update launch (the library's default, or the
+    TTT_GROUP_TOKENS override it honours)."""
+    v = os.environ.get("TTT_GROUP_TOKENS")
+    n = int(v) if v and v.isdigit() else 2048
+    return n if 256 <= n <= 4096 else 2048
+
+
 def kernel_hash() -> str:
     with open(KERNEL_SRC, "rb") as fh:
         return hashlib.sha256(fh.read()).hexdigest()[:16]
@@ -385,7 +393,8 @@ def run_ours(args):
                 "steps": args.steps, "warmup": max(3, args.warmup),
                 "ms_per_step": 1e3 * tmax / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": workload_config(args, {"group_chunks": max(1, 1024 // args.chunk)}),
+                "config": workload_config(args, {"group_tokens": group_tokens(),
+                                                  "group_chunks": max(1, group_tokens() // args.chunk)}),
                 "e2e": e2e, "gpu_launches": prof["launches"] // prof_steps * args.steps,
                 "roofline": roofline,
                 "cpu_baseline": cpu, "clocks": clk.summary(), "path": layer.path}

@@ -324,6 +324,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
   return d;
 }
 
+// The constant (address-free) part of sdesc_sw128(., lbo, sbo): a descriptor
+// for shared-memory address `a` is this value | ((a & 0x3FFFF) >> 4), and
+// advancing the address by `off` bytes adds off >> 4 (the operands lie below
+// 2^18, so the 14-bit start field never carries).
+__host__ __device__ constexpr uint64_t sdesc_sw128_hi(uint32_t lbo, uint32_t sbo) {
+  return (static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16) |
+         (static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
 // 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets lane
 // (base lane + i), columns [col, col+32).  The registers are only valid after
 // tmem_ld_wait(), which takes them as operands so no use is hoisted above it.

@@ -275,14 +275,6 @@ __device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& t
   }
 }
 
-// Operand majors of K block kb: 0 = both K-major, 1 = B MN-major, 2 = both MN-major.
-template <int MODE>
-__device__ __forceinline__ int kblock_layout(const TileInfo& ti, int kb) {
-  if (MODE != kGroup) return 0;
-  if (ti.kind == 1) return 2;
-  return kb < ti.nkb1 ? 0 : 1;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -572,6 +564,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       // ---------------- MMA issuer for the pair
       int stage = 0;
       uint32_t phase = 0;
+      const uint32_t sa_base = smem_u32(stage_base);
+      uint32_t sa_cur = sa_base;  // shared address of ring stage `stage`
       int acc_it = 0;
       bool ok = true;
 #pragma unroll 1
@@ -591,44 +585,77 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           break;
         tc_fence_after();
         const uint32_t tacc = tmem_base + buf * kBN;
-        const int nkb = ti.npre + ti.nkb1 + ti.nkb2;
+        // A tile's ring blocks come in up to three segments of fixed operand
+        // layout: the update tile's fp32 W preload, the main K loop, and the
+        // intra-group correction.  This one thread must keep up with the
+        // tensor pipe (4 MMAs of 128 cycles per block), so everything that
+        // depends only on the segment is hoisted: a block costs a wait, two
+        // ORs, four MMAs with one add each, and a commit.
+        constexpr uint64_t kK = sdesc_sw128_hi(0, 1024), kMN = sdesc_sw128_hi(8192, 1024);
 #pragma unroll 1
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = 0; kb < ti.npre; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, a.err, kErrWaitTmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(stage_base + stage * kStageBytes);
-          if (kb < ti.npre) {
-            // fp32 W boxes (128 rows x 128 B, 128-byte swizzle) -> each CTA's
-            // accumulator columns, 8 columns per copy
-            const int b0 = kb * kWBoxesPerStage, b1 = min(b0 + kWBoxesPerStage, kWBoxes);
-            for (int b = b0; b < b1; ++b) {
-              const uint32_t src = sa + (b - b0) * kWBoxBytes;
+          // fp32 W boxes (128 rows x 128 B, 128-byte swizzle) -> each CTA's
+          // accumulator columns, 8 columns per copy
+          const uint64_t src = kK | ((sa_cur & 0x3FFFFu) >> 4);
+          const int b0 = kb * kWBoxesPerStage, b1 = min(b0 + kWBoxesPerStage, kWBoxes);
+          for (int b = b0; b < b1; ++b) {
 #pragma unroll
-              for (int j = 0; j < kWBoxCols / 8; ++j)
-                tc_cp_128x256b_pair(tacc + b * kWBoxCols + j * 8, sdesc_sw128(src + j * 32, 0, 1024));
-            }
-          } else {
-            const int kk = kb - ti.npre;
-            const uint32_t sb = sa + kABytes;
-            const int lay = kblock_layout<MODE>(ti, kk);
-            const uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, lay == 2, lay >= 1);
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              const uint64_t ad = (lay == 2) ? sdesc_sw128(sa + k * 2048, 8192, 1024)
-                                             : sdesc_sw128(sa + k * 32, 0, 1024);
-              const uint64_t bd = (lay >= 1) ? sdesc_sw128(sb + k * 2048, 8192, 1024)
-                                             : sdesc_sw128(sb + k * 32, 0, 1024);
-              tc_mma_bf16_pair(tacc, ad, bd, idesc, (ti.npre > 0 || kk > 0 || k > 0) ? 1u : 0u);
-            }
+            for (int j = 0; j < kWBoxCols / 8; ++j)
+              tc_cp_128x256b_pair(tacc + b * kWBoxCols + j * 8,
+                                  src + ((uint32_t)((b - b0) * kWBoxBytes + j * 32) >> 4));
           }
-          // the stage is free in both CTAs once the pair's MMAs have read it
           tc_commit_pair_mc(&empty[stage], kPairMask);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
+            sa_cur = sa_base;
+          } else {
+            sa_cur += kStageBytes;
+          }
+        }
+#pragma unroll 1
+        for (int seg = 0; seg < 2 && ok; ++seg) {
+          const int cnt = seg == 0 ? ti.nkb1 : ti.nkb2;
+          // operand majors: 0 both K-major, 1 B MN-major (correction),
+          // 2 both MN-major (update)
+          const int lay = seg == 1 ? 1 : ((MODE == kGroup && ti.kind == 1) ? 2 : 0);
+          const uint32_t idesc = lay == 0   ? idesc_bf16_f32(2 * kBM, kBN, false, false)
+                                 : lay == 1 ? idesc_bf16_f32(2 * kBM, kBN, false, true)
+                                            : idesc_bf16_f32(2 * kBM, kBN, true, true);
+          const uint64_t ahi = lay == 2 ? kMN : kK, bhi = lay >= 1 ? kMN : kK;
+          const uint32_t astep = lay == 2 ? (2048 >> 4) : (32 >> 4);
+          const uint32_t bstep = lay >= 1 ? (2048 >> 4) : (32 >> 4);
+          uint32_t accum = (ti.npre > 0 || seg > 0) ? 1u : 0u;
+#pragma unroll 1
+          for (int i = 0; i < cnt; ++i) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, a.err, kErrWaitTmaFull)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            uint64_t ad = ahi | ((sa_cur & 0x3FFFFu) >> 4);
+            uint64_t bd = bhi | (((sa_cur + kABytes) & 0x3FFFFu) >> 4);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              tc_mma_bf16_pair(tacc, ad, bd, idesc, accum);
+              accum = 1u;
+              ad += astep;
+              bd += bstep;
+            }
+            // the stage is free in both CTAs once the pair's MMAs have read it
+            tc_commit_pair_mc(&empty[stage], kPairMask);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+              sa_cur = sa_base;
+            } else {
+              sa_cur += kStageBytes;
+            }
           }
         }
         if (!ok) break;

@@ -72,6 +72,21 @@ bool force_simt() {
   return f && f[0] == '1';
 }
 
+// Tokens per group of the tcgen05 path.  The fast weight is streamed through
+// HBM once per group while the intra-group correction (Gram blocks) grows with
+// the group; on a B300 at the Qwen3-4B layer shape 2048 measured best (group
+// kernel 75% of the sustained bf16 peak; 1024: 64%, 512: 46%; whole layer
+// +3% over 1024).  The TTT_GROUP_TOKENS environment variable (256..4096) is a
+// tuning override.
+int group_tokens() {
+  static const int g = [] {
+    const char* v = std::getenv("TTT_GROUP_TOKENS");
+    const int n = v ? std::atoi(v) : 2048;
+    return (n >= 256 && n <= 4096) ? n : 2048;
+  }();
+  return g;
+}
+
 struct Layout {
   bool tc;
   int G, L, s_pad, s_slots;
@@ -108,7 +123,7 @@ Layout make_layout(const ttt_mlp_config& c, bool tc) {
   const size_t act = (c.act_dtype == TTT_BF16) ? 2 : 4;
   const size_t inter = tc ? 2 : 4;
   const size_t d = c.d, f = c.f, n = (size_t)c.max_tokens;
-  l.G = tc ? std::max(1, 1024 / c.chunk) : 1;
+  l.G = tc ? std::max(1, group_tokens() / c.chunk) : 1;
   l.L = l.G * c.chunk;
   l.s_pad = (int)align_up((size_t)l.L, 256);
   l.s_slots = tc ? (int)std::min<int64_t>(kMaxGroups, (c.max_tokens + l.L - 1) / l.L + 4) : 0;
