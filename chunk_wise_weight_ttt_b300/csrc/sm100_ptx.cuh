@@ -173,6 +173,15 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       : "memory");
 }
 
+// Prefetch one box of a tensor map into L2 (no shared memory is written and
+// nothing is signalled); coordinates as for tma_load_2d.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 //
 // Kernels that pair two CTAs on one MMA use the cta_group::2 forms below for
@@ -246,11 +255,6 @@ __device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc
       : "memory");
 }
 
-// Pair form of tc_cp_128x256b: each CTA's block at the descriptor's offset goes
-// to its own TMEM.
-__device__ __forceinline__ void tc_cp_128x256b_pair(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
 
 // Pair forms of the commits: arrive once on `bar` in this CTA, or at `bar`'s
 // offset in every CTA of `cta_mask`, when the pair's tcgen05 ops issued so
@@ -269,15 +273,6 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint64_t* bar, uint16_t cta_ma
       : "memory");
 }
 
-// Copy a 128-row x 256-bit block (8 fp32 columns per row) from shared memory
-// into TMEM: smem row r -> TMEM lane r, columns [taddr.col, taddr.col + 8).
-// The source is described by a shared-memory matrix descriptor exactly like an
-// MMA operand (here K-major with 128-byte swizzle), and the copy is ordered with
-// the tcgen05.mma ops issued before and after it by the same thread.  One
-// thread issues.
-__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
 
 // Arrive (once) on `bar` when every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {

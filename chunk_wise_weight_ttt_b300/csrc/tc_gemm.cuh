@@ -35,11 +35,12 @@
 //              O_g = Z_g W_s^T + S_g V_g            (W_s = state at group start)
 //            and the update tiles
 //              W <- W_s + V_g^T Z_g,  Wb_next <- bf16(W)
-//            in one launch.  An update tile first streams its fp32 block of
-//            W_s through the operand ring into the TMEM accumulators
-//            (tcgen05.cp), so the MMAs accumulate straight onto the fast
-//            weight and the epilogue only stores (W and its bf16 copy),
-//            coalesced through a per-warp shared-memory transpose.
+//            in one launch.  An update tile accumulates V_g^T Z_g from zero
+//            in TMEM; its epilogue adds the fp32 block of W_s in one rounding
+//            (read in a coalesced layout, one 32-column slice ahead, after the
+//            producer prefetched it into L2 at the tile's start) and stores W
+//            and its bf16 copy, coalesced through a per-warp shared-memory
+//            transpose.
 //            Applying W_s to every chunk of the group plus the intra-group
 //            correction S_g V_g equals applying each chunk's own pre-update
 //            state (the deltas are additive, appendix B of the "In-Place
@@ -67,13 +68,9 @@ constexpr int kGemmThreads = 192;
 constexpr int kMaxGroups = 256;
 constexpr int kSwizzlePairs = 8;   // SwiGLU raster: tile pairs per column sweep
 constexpr uint16_t kPairMask = 0x3;  // both CTAs of the cluster
-// fp32 fast-weight preload of an update tile: boxes of 32 columns x 128 rows
-// (128-byte rows, 16 KB), two per ring stage.
+// An update tile's fp32 W block, as L2-prefetch boxes of 32 columns x 128 rows.
 constexpr int kWBoxCols = 32;
-constexpr int kWBoxBytes = kBM * kWBoxCols * 4;
-constexpr int kWBoxesPerStage = kStageBytes / kWBoxBytes;
 constexpr int kWBoxes = kBN / kWBoxCols;
-constexpr int kWPreBlocks = (kWBoxes + kWBoxesPerStage - 1) / kWBoxesPerStage;
 // per-warp staging for the transposed (coalesced) update-tile stores
 constexpr int kStgBytesPerWarp = 32 * 128;
 constexpr int kEpiWarps = 4;
@@ -112,7 +109,6 @@ struct TileInfo {
   int kind;  // 0 plain/apply, 1 update
   int m0, n0;
   int g;
-  int npre;        // leading ring blocks that preload the accumulator (update tiles)
   int nkb1, nkb2;  // MMA K blocks: main operands, then the intra-group correction
   bool valid;
 };
@@ -147,7 +143,6 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int ra
   TileInfo ti{};
   ti.valid = true;
   ti.nkb2 = 0;
-  ti.npre = 0;
   ti.kind = 0;
   ti.g = 0;
   if (MODE == kSwiGLU) {
@@ -206,40 +201,23 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int ra
       ti.kind = 1;
       ti.m0 = (2 * (u / ntU) + rank) * kBM;
       ti.n0 = (u % ntU) * kBN;
-      ti.npre = kWPreBlocks;
       ti.nkb1 = cdiv(a.glen, kBK);
     }
   }
   return ti;
 }
 
-// Bytes that ring block `kb` of the pair's tiles brings into both CTAs (what
+// Bytes that one ring block of the pair's tiles brings into both CTAs (what
 // the leader's full barrier expects).
-template <int MODE>
-__device__ __forceinline__ uint32_t kblock_bytes(const TileInfo& ti, int kb) {
-  if (MODE == kGroup && kb < ti.npre)
-    return 2u * static_cast<uint32_t>(min(kWBoxesPerStage, kWBoxes - kb * kWBoxesPerStage)) *
-           kWBoxBytes;
-  return 2u * kStageBytes;
-}
+constexpr uint32_t kBlockBytesPair = 2u * kStageBytes;
 
 // Issue this CTA's TMA loads of ring block `kb` of tile `ti` into stage
 // buffers sa / sb: its A rows and its half (`rank`) of the B block, with
 // completion signalled on the leader's barrier `bar` (a shared::cluster
-// address).  For an update tile the first npre blocks are this CTA's fp32 W
-// boxes, then the K blocks of the operands.
+// address).
 template <int MODE>
 __device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& ti, int kb, int rank,
                                             uint8_t* sa, uint8_t* sb, uint32_t bar) {
-  if (MODE == kGroup && ti.kind == 1) {
-    if (kb < ti.npre) {
-      const int b0 = kb * kWBoxesPerStage, b1 = min(b0 + kWBoxesPerStage, kWBoxes);
-      for (int b = b0; b < b1; ++b)
-        tma_load_2d_pair(sa + (b - b0) * kWBoxBytes, &a.map[6], bar, ti.n0 + b * kWBoxCols, ti.m0);
-      return;
-    }
-    kb -= ti.npre;
-  }
   const int kh = kBN / 2;  // B rows (or MN columns) per half
   if (MODE == kSwiGLU) {
     tma_load_2d_pair(sa, &a.map[0], bar, kb * kBK, ti.m0);
@@ -264,7 +242,7 @@ __device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& t
           tma_load_2d_pair(sb + q * 8192, &a.map[3], bar, ti.n0 + rank * kh + q * 64, a.g0 + k2);
       }
     } else {
-      const int k = a.g0 + kb * kBK;  // kb already excludes the preload blocks
+      const int k = a.g0 + kb * kBK;
 #pragma unroll
       for (int q = 0; q < kBM / 64; ++q)
         tma_load_2d_pair(sa + q * 8192, &a.map[4], bar, ti.m0 + q * 64, k);
@@ -281,6 +259,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+// 16-byte global load cached in L2 only.
+__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
                                              uint32_t w) {
@@ -334,17 +321,33 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
     }
   } else if (MODE == kVProj || MODE == kGroup) {
     if (MODE == kGroup && ti.kind == 1) {
-      // fast-weight update: the accumulator already holds W_s + V^T Z.  Each
-      // 32-column slice of the warp's 32 rows goes registers -> staging
-      // (row per thread, 16-byte chunks XOR-swizzled by row so both phases are
-      // bank-conflict free) -> 4 full rows per store instruction.
+      // fast-weight update: W <- W_s + acc (acc = V^T Z of the group, from
+      // zero), one fp32 rounding.  Each 32-column slice of the warp's 32 rows
+      // goes TMEM -> registers (row per thread) -> staging (16-byte chunks
+      // XOR-swizzled by row, so both phases are bank-conflict free) -> the
+      // coalesced layout (4 full rows per instruction), where the thread adds
+      // W_s, read in that same layout one slice ahead, and stores W and its
+      // bf16 copy.
       const int lane = row & 31;
       const int rbase = ti.m0 + (row - lane);
       float* W = reinterpret_cast<float*>(a.out1);
       __nv_bfloat16* Wb = reinterpret_cast<__nv_bfloat16*>(a.out2);
       const uint32_t st_row = smem_u32(stg) + lane * 128;
-#pragma unroll 1
+      const int cq = lane & 7;
+      float4 wc[8], wn[8];
+      auto load_w = [&](int s, float4 (&dst)[8]) {
+        const int col = ti.n0 + s * 32 + cq * 4;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int wr = rbase + j * 4 + (lane >> 3);
+          dst[j] = (wr < a.d && col < a.f) ? ld_cg_f4(W + (size_t)wr * a.f + col)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      };
+      load_w(0, wc);
+#pragma unroll
       for (int s = 0; s < kBN / 32; ++s) {
+        if (s + 1 < kBN / 32) load_w(s + 1, wn);
         tmem_ld32(tacc + s * 32, r);
         tmem_ld_wait(r);
 #pragma unroll
@@ -352,7 +355,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
           st_shared_v4(st_row + ((q ^ (lane & 7)) << 4), r[4 * q], r[4 * q + 1], r[4 * q + 2],
                        r[4 * q + 3]);
         __syncwarp();
-        const int cq = lane & 7;
         const int col = ti.n0 + s * 32 + cq * 4;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -361,13 +363,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
           ld_shared_v4(smem_u32(stg) + rr * 128 + ((cq ^ (rr & 7)) << 4), v);
           const int wr = rbase + rr;
           if (wr < a.d && col < a.f) {
-            *reinterpret_cast<uint4*>(W + (size_t)wr * a.f + col) = make_uint4(v[0], v[1], v[2], v[3]);
+            const float4 w = make_float4(wc[j].x + __uint_as_float(v[0]), wc[j].y + __uint_as_float(v[1]),
+                                         wc[j].z + __uint_as_float(v[2]), wc[j].w + __uint_as_float(v[3]));
+            *reinterpret_cast<float4*>(W + (size_t)wr * a.f + col) = w;
             *reinterpret_cast<uint2*>(Wb + (size_t)wr * a.f + col) =
-                make_uint2(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
-                           pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])));
+                make_uint2(pack_bf16x2(w.x, w.y), pack_bf16x2(w.z, w.w));
           }
         }
         __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) wc[j] = wn[j];
       }
     } else {
       // plain bf16 store of alpha * acc (kVProj) or acc (kGroup apply)
@@ -533,7 +538,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         if (t >= ntiles) break;
         const TileInfo ti = decode_tile<MODE>(a, t, rank);
         if (!ti.valid) continue;
-        const int nkb = ti.npre + ti.nkb1 + ti.nkb2;
+        if (MODE == kGroup && ti.kind == 1) {
+          // the epilogue adds this tile's fp32 W block after the MMAs; bring
+          // it into L2 now so those reads hit there
+          for (int b = 0; b < kWBoxes; ++b)
+            tma_prefetch_l2_2d(&a.map[6], ti.n0 + b * kWBoxCols, ti.m0);
+        }
+        const int nkb = ti.nkb1 + ti.nkb2;
 #pragma unroll 1
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.err, kErrWaitSmemEmpty)) {
@@ -541,7 +552,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             break;
           }
           uint8_t* sa = stage_base + stage * kStageBytes;
-          if (leader) mbar_arrive_expect_tx(&full[stage], kblock_bytes<MODE>(ti, kb));
+          if (leader) mbar_arrive_expect_tx(&full[stage], kBlockBytesPair);
           load_kblock<MODE>(a, ti, kb, rank, sa, sa + kABytes, cluster_map(smem_u32(&full[stage]), 0));
           ++fills;
           if (++stage == kStages) {
@@ -585,39 +596,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           break;
         tc_fence_after();
         const uint32_t tacc = tmem_base + buf * kBN;
-        // A tile's ring blocks come in up to three segments of fixed operand
-        // layout: the update tile's fp32 W preload, the main K loop, and the
-        // intra-group correction.  This one thread must keep up with the
+        // A tile's ring blocks come in up to two segments of fixed operand
+        // layout: the main K loop and the intra-group correction.  This one thread must keep up with the
         // tensor pipe (4 MMAs of 128 cycles per block), so everything that
         // depends only on the segment is hoisted: a block costs a wait, two
         // ORs, four MMAs with one add each, and a commit.
         constexpr uint64_t kK = sdesc_sw128_hi(0, 1024), kMN = sdesc_sw128_hi(8192, 1024);
-#pragma unroll 1
-        for (int kb = 0; kb < ti.npre; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, a.err, kErrWaitTmaFull)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // fp32 W boxes (128 rows x 128 B, 128-byte swizzle) -> each CTA's
-          // accumulator columns, 8 columns per copy
-          const uint64_t src = kK | ((sa_cur & 0x3FFFFu) >> 4);
-          const int b0 = kb * kWBoxesPerStage, b1 = min(b0 + kWBoxesPerStage, kWBoxes);
-          for (int b = b0; b < b1; ++b) {
-#pragma unroll
-            for (int j = 0; j < kWBoxCols / 8; ++j)
-              tc_cp_128x256b_pair(tacc + b * kWBoxCols + j * 8,
-                                  src + ((uint32_t)((b - b0) * kWBoxBytes + j * 32) >> 4));
-          }
-          tc_commit_pair_mc(&empty[stage], kPairMask);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
-            sa_cur = sa_base;
-          } else {
-            sa_cur += kStageBytes;
-          }
-        }
 #pragma unroll 1
         for (int seg = 0; seg < 2 && ok; ++seg) {
           const int cnt = seg == 0 ? ti.nkb1 : ti.nkb2;
@@ -630,7 +614,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           const uint64_t ahi = lay == 2 ? kMN : kK, bhi = lay >= 1 ? kMN : kK;
           const uint32_t astep = lay == 2 ? (2048 >> 4) : (32 >> 4);
           const uint32_t bstep = lay >= 1 ? (2048 >> 4) : (32 >> 4);
-          uint32_t accum = (ti.npre > 0 || seg > 0) ? 1u : 0u;
+          uint32_t accum = seg > 0 ? 1u : 0u;
 #pragma unroll 1
           for (int i = 0; i < cnt; ++i) {
             if (!mbar_wait(&full[stage], phase, abort_flag, a.err, kErrWaitTmaFull)) {
