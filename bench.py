@@ -231,11 +231,18 @@ def oracle_sample(cfg, seconds: float, min_chunks: int = 2):
 
 # ---------------------------------------------------------------- arms
 
-def make_workload(args, rank: int):
+def workload_x_seed(rank: int, world: int):
+    """Seed of a rank's document X: the single-GPU workload uses the qwen
+    recipe (X drawn first from seed 0); with several ranks every rank draws its
+    own document from 1000 + rank after the shared weights (seed 0)."""
+    return None if world == 1 else 1000 + rank
+
+
+def make_workload(args, rank: int, world: int = 1):
     from ttt_inputs import CONFIGS, make_layer
     c = dict(CONFIGS["qwen"])
     return make_layer(c["d"], c["f"], args.tokens, args.chunk, c["k"], c["eta"], dtype="bf16",
-                      seed=0, init="qwen", x_seed=None if rank == 0 else 1000 + rank)
+                      seed=0, init="qwen", x_seed=workload_x_seed(rank, world))
 
 
 def workload_config(args, extra=None):
@@ -294,7 +301,7 @@ def run_ours(args):
         build()
     barrier(world, dev)
 
-    cfg = make_workload(args, rank)
+    cfg = make_workload(args, rank, world)
     T, d, f = cfg["T"], cfg["d"], cfg["f"]
 
     def t(a):

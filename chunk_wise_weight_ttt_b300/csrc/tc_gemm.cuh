@@ -103,6 +103,9 @@ struct GemmArgs {
   int g_start[kMaxGroups];
   int g_len[kMaxGroups];
   int g0, glen, gslot;  // kGroup
+  // failure-detection test hook: the leader of the pair that claims tile 0
+  // withholds that tile's first ring block, so its bounded waits run out
+  int test_withhold_block;
 };
 
 struct TileInfo {
@@ -553,7 +556,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
           }
           uint8_t* sa = stage_base + stage * kStageBytes;
           if (leader) mbar_arrive_expect_tx(&full[stage], kBlockBytesPair);
-          load_kblock<MODE>(a, ti, kb, rank, sa, sa + kABytes, cluster_map(smem_u32(&full[stage]), 0));
+          if (!(a.test_withhold_block && leader && t == 0 && kb == 0))
+            load_kblock<MODE>(a, ti, kb, rank, sa, sa + kABytes, cluster_map(smem_u32(&full[stage]), 0));
           ++fills;
           if (++stage == kStages) {
             stage = 0;

@@ -418,8 +418,10 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
   a.out0 = h->V;
   a.alpha = c.eta;
   a.counter = next_counter(h, st);
+  a.test_withhold_block = fault_injected("kernel_wait") ? 1 : 0;
   pt.begin(2);
   TTT_CK(h, launch_gemm<kVProj>(h, a, cdiv_h(cdiv_h((int)n, kBM), 2) * cdiv_h(d, kBN), st));
+  a.test_withhold_block = 0;
   pt.end();
   h->prof_launches++;
 

@@ -45,6 +45,12 @@
  *   - Setting the environment variable TTT_FAULT to one of
  *     create|forward|reset|get|set|check makes that call fail with
  *     TTT_EFAULT_INJECTED before it does anything (host-side fault injection).
+ *     TTT_FAULT=kernel_wait instead makes the next forward call's
+ *     target-projection kernel withhold one of its own operand loads, so
+ *     that kernel's bounded waits run out (about 4 s): the call itself
+ *     succeeds, ttt_mlp_check then reports TTT_ETIMEOUT, and the slot's fast
+ *     weight is undefined until it is reset.  (Tests the failure path
+ *     without faulting the GPU.)
  */
 #ifndef TTT_MLP_H
 #define TTT_MLP_H

@@ -207,13 +207,10 @@ def test_update_clipping_simt_fp32():
 
 def test_update_clipping_at_the_pages_threshold():
     """tau = 1e-5 (the pages' long-context evaluation): every delta is clipped
-    to norm 1e-5.  O and W meet the bf16 bounds.  The accumulated update
-    W - W_0 is then only ~15 fp32 ulps of W per element per chunk; the group
-    kernel adds each MMA step's partial sums onto W held in the TMEM
-    accumulator, so its relative error there is large (the apply's bf16 copy
-    of W, 2^-9 relative, hides such updates from O in any case).  It is
-    reported, and bounded only loosely: the direction of the update must
-    still be right."""
+    to norm 1e-5, only a few fp32 ulps of W per element.  The group's delta is
+    accumulated from zero and added to W in one rounding, so the accumulated
+    update W - W_0 itself matches the oracle's (bound 5e-2: fp32 W rounds each
+    group's addition)."""
     cfg = _bf16_cfg(T=1024, C=128, seed=5)
     layer, dt = _make_gpu_layer(cfg, clip_tau=1e-5)
     o = layer.forward(_dev(cfg["x"], dt), doc_starts=(0,))
@@ -227,7 +224,7 @@ def test_update_clipping_at_the_pages_threshold():
                 (np.linalg.norm(w - w0) * np.linalg.norm(w_ref - w0)))
     print(f"tau=1e-5: |W - W0| {np.linalg.norm(w_ref - w0):.3e}, W err {_rel(w, w_ref):.3e}, "
           f"error of W - W0 {err:.3e}, cosine {cos:.4f}")
-    assert cos >= 0.8
+    assert err <= 5e-2 and cos >= 0.999
 
 
 def test_empty_call_and_token_limit():
@@ -346,6 +343,34 @@ def test_fault_injection_leaves_handle_usable(monkeypatch):
     o = layer.forward(x)
     o_ref, _ = _oracle(cfg)
     assert _rel(_host(o), o_ref) < TOL_BF16
+
+
+def test_bounded_wait_runs_out_and_handle_recovers(monkeypatch):
+    """TTT_FAULT=kernel_wait makes the target-projection kernel withhold one of
+    its own operand loads: the barrier that waits for it never completes, the
+    kernel's bounded waits run out (no GPU fault, no hang), ttt_mlp_check
+    reports TTT_ETIMEOUT, and after a reset the handle computes correctly."""
+    import time
+    from chunk_wise_weight_ttt_b300 import TTTError
+    cfg = _bf16_cfg(T=512, C=64)
+    layer, dt = _make_gpu_layer(cfg)
+    x = _dev(cfg["x"], dt)
+    layer.check()
+    monkeypatch.setenv("TTT_FAULT", "kernel_wait")
+    t0 = time.time()
+    layer.forward(x)  # enqueued: the failure is asynchronous
+    monkeypatch.delenv("TTT_FAULT")
+    with pytest.raises(TTTError, match="ETIMEOUT"):
+        layer.check()
+    elapsed = time.time() - t0
+    print(f"bounded waits ran out after {elapsed:.1f} s")
+    assert 1.0 < elapsed < 60.0
+    layer.check()  # the error word was cleared
+    layer.reset()
+    o = layer.forward(x)
+    o_ref, _ = _oracle(cfg)
+    assert _rel(_host(o), o_ref) < TOL_BF16
+    layer.check()
 
 
 def test_rmsnorm_and_residual_glue():
