@@ -61,46 +61,86 @@ struct SpanList {
 
 // U[t] = sum_{j<k} conv[j] (.) X0[t + off(j)] with every term outside t's
 // chunk dropped (chunk-local depthwise Conv1D); off(j) = 1 + j (next-token
-// window), j (current-token window) or 1 - j (causal window), by `mode`.  One
-// thread per (token, 8 channels), vector loads and stores (rows are 16-byte
-// aligned: d is a multiple of 8).  Tokens outside every span are untouched.
+// window), j (current-token window) or 1 - j (causal window), by `mode`.
+// A CTA (256 threads) computes conv_tokens<TIn>() consecutive tokens x
+// kConvCh channels of the tokens covered by `spans`: it stages the X0 rows
+// those tokens read (tokens + k - 1 rows) in shared memory with asynchronous
+// 16-byte copies (all in flight at once; zero-filled outside the spans), so
+// every row comes from HBM once, then each thread computes 8 channels of
+// tokens / 8 tokens.  Tokens outside every span are untouched.
+// Grid: (ceil(span tokens / conv_tokens<TIn>()), ceil(d / kConvCh)).
+constexpr int kConvCh = 256;
+template <typename TIn>
+__host__ __device__ constexpr int conv_tokens() { return sizeof(TIn) == 2 ? 64 : 32; }
+
+// 16-byte asynchronous global -> shared copy; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gmem_src), "r"(src_bytes)
+               : "memory");
+}
+
 template <typename TIn, typename TOut>
-__global__ void conv_target_kernel(const TIn* __restrict__ x0, const TIn* __restrict__ conv_w,
-                                   TOut* __restrict__ u, int d, int k, const SpanList spans,
-                                   int mode) {
-  const int groups_per_row = d / 8;
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+__global__ void __launch_bounds__(256) conv_target_kernel(const TIn* __restrict__ x0,
+                                                          const TIn* __restrict__ conv_w,
+                                                          TOut* __restrict__ u, int d, int k,
+                                                          const SpanList spans, int mode) {
+  constexpr int kConvTok = conv_tokens<TIn>();
+  constexpr int kConvRows = kConvTok + 8;  // k <= 8
+  __shared__ __align__(16) TIn slab[kConvRows * kConvCh];
   const int first = spans.start[0];
-  const long long total =
-      (long long)(spans.start[spans.n - 1] + spans.len[spans.n - 1] - first) * groups_per_row;
-  if (idx >= total) return;
-  const int t = first + (int)(idx / groups_per_row);
-  const int c0 = (int)(idx % groups_per_row) * 8;
-  int lo = 0, hi = spans.n - 1;
-  while (lo < hi) {  // last span starting at or before t
-    const int mid = (lo + hi + 1) / 2;
-    if (spans.start[mid] <= t) lo = mid; else hi = mid - 1;
+  const int last = spans.start[spans.n - 1] + spans.len[spans.n - 1];  // exclusive
+  const int t0 = first + blockIdx.x * kConvTok;
+  const int ch0 = blockIdx.y * kConvCh;
+  const int omin = (mode == 2) ? 2 - k : (mode == 1 ? 0 : 1);  // smallest tap offset
+  const int nrows = kConvTok + k - 1;
+  constexpr int kChunks = kConvCh / 8;                 // groups of 8 channels per row
+  constexpr int kPieces = 8 * (int)sizeof(TIn) / 16;   // 16-byte copies per group
+  for (int q = threadIdx.x; q < nrows * kChunks * kPieces; q += blockDim.x) {
+    const int pc = q % kPieces, rc = q / kPieces;
+    const int r = rc / kChunks, cg = rc % kChunks;
+    const int row = t0 + omin + r, ch = ch0 + cg * 8;
+    const bool in = row >= first && row < last && ch < d;
+    const TIn* src = in ? x0 + (size_t)row * d + ch : x0;
+    cp_async16(slab + r * kConvCh + cg * 8 + pc * (16 / (int)sizeof(TIn)),
+               reinterpret_cast<const uint8_t*>(src) + pc * 16, in ? 16 : 0);
   }
-  const int s0 = spans.start[lo];
-  const int cbeg = s0 + ((t - s0) / spans.chunk) * spans.chunk;
-  const int cend = min(cbeg + spans.chunk, s0 + spans.len[lo]);
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  const int cg = threadIdx.x % kChunks, tl = threadIdx.x / kChunks;
+  const int ch = ch0 + cg * 8;
+  if (ch >= d) return;
   const int base = (mode == 1) ? 0 : 1;
   const int step = (mode == 2) ? -1 : 1;
-  float acc[8];
+  for (int i = tl; i < kConvTok; i += 256 / kChunks) {
+    const int t = t0 + i;
+    if (t >= last) break;
+    int lo = 0, hi = spans.n - 1;
+    while (lo < hi) {  // last span starting at or before t
+      const int mid = (lo + hi + 1) / 2;
+      if (spans.start[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int s0 = spans.start[lo];
+    if (t >= s0 + spans.len[lo]) continue;  // in a gap between spans
+    const int cbeg = s0 + ((t - s0) / spans.chunk) * spans.chunk;
+    const int cend = min(cbeg + spans.chunk, s0 + spans.len[lo]);
+    float acc[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    const int src = t + base + step * j;
-    if (src < cbeg || src >= cend) continue;
-    const TIn* xr = x0 + (size_t)src * d + c0;
-    const TIn* wr = conv_w + (size_t)j * d + c0;
-    float xv[8], wv[8];
-    load8(xr, xv);
-    load8(wr, wv);
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = fmaf(wv[e], xv[e], acc[e]);
+    for (int j = 0; j < 8; ++j) {
+      const int src = t + base + step * j;
+      if (j < k && src >= cbeg && src < cend) {
+        float xv[8], wv[8];
+        load8(slab + (src - t0 - omin) * kConvCh + cg * 8, xv);
+        load8(conv_w + (size_t)j * d + ch, wv);  // L1-resident: k x 16 bytes per thread
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(wv[e], xv[e], acc[e]);
+      }
+    }
+    store8(u + (size_t)t * d + ch, acc);
   }
-  store8(u + (size_t)t * d + c0, acc);
 }
 
 // C(m,n) = alpha * sum_k A(m,k) B(k,n) + beta * C(m,n), fp32 accumulation.

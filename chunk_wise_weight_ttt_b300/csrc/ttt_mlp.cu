@@ -220,6 +220,14 @@ ttt_status fail(ttt_mlp* h, ttt_status s, const std::string& msg) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Launch shape of conv_target_kernel<TIn, .> for the tokens the span list covers.
+template <typename TIn>
+dim3 conv_grid(const SpanList& sl, int d) {
+  const int ntok = sl.start[sl.n - 1] + sl.len[sl.n - 1] - sl.start[0];
+  constexpr int tok = conv_tokens<TIn>();
+  return dim3((unsigned)((ntok + tok - 1) / tok), (unsigned)((d + kConvCh - 1) / kConvCh));
+}
+
 int grid_for(long long n, int block) {
   long long g = (n + block - 1) / block;
   return (int)std::max<long long>(1, std::min<long long>(g, 1 << 20));
@@ -383,8 +391,7 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
       sl.start[i - w0] = groups[i].start;
       sl.len[i - w0] = groups[i].len;
     }
-    const long long cnt = (long long)(groups[w1 - 1].start + groups[w1 - 1].len - groups[w0].start) * (d / 8);
-    conv_target_kernel<__nv_bfloat16, __nv_bfloat16><<<grid_for(cnt, 256), 256, 0, st>>>(
+    conv_target_kernel<__nv_bfloat16, __nv_bfloat16><<<conv_grid<__nv_bfloat16>(sl, d), 256, 0, st>>>(
         (const __nv_bfloat16*)x0, (const __nv_bfloat16*)h->conv, (__nv_bfloat16*)h->U, d, c.conv_k, sl,
         c.target_mode);
     TTT_CK_LAUNCH(h);
@@ -568,8 +575,7 @@ ttt_status forward_simt_t(ttt_mlp* h, int doc, const void* xv, const void* x0v, 
       sl.start[i - w0] = spans[i].start;
       sl.len[i - w0] = spans[i].len;
     }
-    const long long cnt = (long long)(spans[w1 - 1].start + spans[w1 - 1].len - spans[w0].start) * (d / 8);
-    conv_target_kernel<T, float><<<grid_for(cnt, 256), 256, 0, st>>>(x0, (const T*)h->conv, U, d, c.conv_k, sl,
+    conv_target_kernel<T, float><<<conv_grid<T>(sl, d), 256, 0, st>>>(x0, (const T*)h->conv, U, d, c.conv_k, sl,
                                                                      c.target_mode);
     TTT_CK_LAUNCH(h);
     h->prof_launches++;
@@ -1040,8 +1046,7 @@ extern "C" ttt_status ttt_target_noalloc(const void* x0, const void* conv_w, con
       sl.start[i - w0] = docs[i].start;
       sl.len[i - w0] = docs[i].len;
     }
-    const long long cnt = (long long)(docs[w1 - 1].start + docs[w1 - 1].len - docs[w0].start) * (d / 8);
-    conv_target_kernel<__nv_bfloat16, __nv_bfloat16><<<grid_for(cnt, 256), 256, 0, st>>>(
+    conv_target_kernel<__nv_bfloat16, __nv_bfloat16><<<conv_grid<__nv_bfloat16>(sl, d), 256, 0, st>>>(
         (const __nv_bfloat16*)x0, (const __nv_bfloat16*)conv_w, u, d, conv_k, sl, /*mode=*/0);
     TTT_CK(nullptr, cudaGetLastError());
   }
