@@ -55,6 +55,10 @@ def parse_args(argv=None):
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--workload", choices=["layer", "long", "sweep", "stack"], default="layer",
+                   help="layer: the headline workload (default, one JSON line with the full "
+                        "contract); long / sweep / stack: the other measured configurations, "
+                        "one JSON line per case (device-timed, inputs drawn on the GPU)")
     return p.parse_args(argv)
 
 
@@ -413,10 +417,95 @@ def run_ours(args):
     return 0
 
 
+def run_extra(args):
+    """The other configurations of the layer, timed on one GPU with inputs
+    resident in HBM (drawn with torch's device generator: weights N(0, 0.02^2),
+    X rows RMS-normalised; timing only, no oracle).  One JSON line per case."""
+    import torch
+    from chunk_wise_weight_ttt_b300 import TTTMLP, TTTStack
+    from chunk_wise_weight_ttt_b300.build import build
+    from ttt_inputs import CONFIGS, make_stack_device
+    build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+
+    def weights(d, f, k, seed):
+        g = torch.Generator(device=dev).manual_seed(seed)
+        nrm = lambda *sh: (torch.randn(*sh, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        return [nrm(f, d), nrm(f, d), nrm(d, f), nrm(k, d), nrm(d, d)]
+
+    def tokens(T, d, seed):
+        g = torch.Generator(device=dev).manual_seed(seed)
+        x = torch.randn(T, d, generator=g, device=dev)
+        return (x / torch.sqrt(x.pow(2).mean(1, keepdim=True) + 1e-6)).to(torch.bfloat16)
+
+    def timed(fn, steps, warmup):
+        for _ in range(max(3, warmup)):
+            fn()
+        torch.cuda.synchronize(dev)
+        with ClockSampler(0) as clk:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / 1e3 / steps, clk.summary()
+
+    def emit(name, tok, sec, clocks, config):
+        print(json.dumps({"metric": f"TTT-MLP tokens/s, {name}", "value": tok / sec,
+                          "unit": UNIT, "ms_per_step": 1e3 * sec, "higher_is_better": True,
+                          "dtype": "bf16", "data": "synthetic", "n_gpus": 1,
+                          "config": config, "clocks": clocks}), flush=True)
+
+    steps = max(3, min(args.steps, 20))
+    if args.workload == "long":
+        c = CONFIGS["long"]
+        layer = TTTMLP(*weights(c["d"], c["f"], c["k"], 0), chunk=c["chunk"], eta=c["eta"],
+                       max_tokens=c["T"])
+        x = tokens(c["T"], c["d"], 1)
+        o = torch.empty_like(x)
+        sec, clk = timed(lambda: layer.forward(x, doc_starts=c["doc_starts"], out=o), steps,
+                         args.warmup)
+        layer.check()
+        emit("131072-token call with a document every 32768 tokens", c["T"], sec, clk,
+             {"workload": "long", "d": c["d"], "f": c["f"], "T": c["T"], "chunk": c["chunk"],
+              "doc_starts": list(c["doc_starts"])})
+    elif args.workload == "sweep":
+        c = CONFIGS["sweep"]
+        xs = [tokens(c["T"], c["d"], 1000 + b) for b in range(8)]
+        outs = [torch.empty_like(x) for x in xs]
+        w = weights(c["d"], c["f"], c["k"], 0)
+        for C in (64, 128, 256, 512, 1024):
+            layer = TTTMLP(*w, chunk=C, eta=c["eta"], n_docs=8, max_tokens=c["T"])
+            for B in (1, 4, 8):
+                def step():
+                    for b in range(B):
+                        layer.forward(xs[b], doc=b, doc_starts=(0,), out=outs[b])
+                sec, clk = timed(step, steps, args.warmup)
+                layer.check()
+                emit(f"C={C}, batch {B} documents of {c['T']} tokens", B * c["T"], sec, clk,
+                     {"workload": "sweep", "d": c["d"], "f": c["f"], "T_per_doc": c["T"],
+                      "chunk": C, "batch": B})
+            layer.close()
+    else:
+        c = CONFIGS["stack"]
+        h0, layers = make_stack_device(c["n_layers"], c["d"], c["f"], c["T"], c["k"], seed=0)
+        stack = TTTStack(layers, chunk=c["chunk"], eta=c["eta"], max_tokens=c["T"])
+        sec, clk = timed(lambda: stack(h0), max(3, min(steps, 5)), 1)
+        emit(f"{c['n_layers']}-layer stack (tokens through all layers)", c["T"], sec, clk,
+             {"workload": "stack", "n_layers": c["n_layers"], "d": c["d"], "f": c["f"],
+              "T": c["T"], "chunk": c["chunk"],
+              "layer_tokens_per_s": c["n_layers"] * c["T"] / sec})
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != "layer":
+        return run_extra(args)
     return run_ours(args)
 
 
