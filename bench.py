@@ -117,8 +117,8 @@ def load_peaks():
 
 
 def group_tokens() -> int:
-    """Tokens per fused apply+update launch (the library's default, or the
-    TTT_GROUP_TOKENS override it honours)."""
+    """Target tokens per group of the fused apply+update kernel (the library's
+    default, or the TTT_GROUP_TOKENS override it honours)."""
     v = os.environ.get("TTT_GROUP_TOKENS")
     n = int(v) if v and v.isdigit() else 2048
     return n if 256 <= n <= 4096 else 2048
@@ -129,16 +129,20 @@ def kernel_hash() -> str:
         return hashlib.sha256(fh.read()).hexdigest()[:16]
 
 
-def stored_traffic():
-    """DRAM bytes per group-kernel launch from the committed ncu summary, or
-    None when the kernel source has changed since the counters were taken."""
+def stored_traffic(groups_per_launch: float, chunk: int, d: int, f: int):
+    """DRAM bytes per group-kernel launch: the committed ncu figure per group
+    times the groups one launch chains.  None when the kernel source has
+    changed since the counters were taken, or for a shape or grouping other
+    than the captured one."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as fh:
-        d = json.load(fh)
-    if d.get("kernel_sha256_16") != kernel_hash():
+        rec = json.load(fh)
+    if (rec.get("kernel_sha256_16") != kernel_hash() or "dram_bytes_per_group" not in rec
+            or rec.get("captured_chunk") != chunk or rec.get("captured_group_tokens") != group_tokens()
+            or rec.get("captured_shape") != {"d": d, "f": f}):
         return None
-    return d.get("dram_bytes_per_launch")
+    return rec["dram_bytes_per_group"] * groups_per_launch
 
 
 class ClockSampler:
@@ -379,7 +383,9 @@ def run_ours(args):
     flops = 4.0 * prof_steps * T * d * f          # algorithmic apply + update FLOPs
     achieved = flops / group_s / 1e12 if group_s > 0 else None
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    traffic = stored_traffic()
+    group_len = max(1, group_tokens() // args.chunk) * args.chunk
+    groups_per_step = -(-T // group_len)
+    traffic = stored_traffic(groups_per_step * prof_steps / n_launch, args.chunk, d, f)
     roofline = {"bound": "tensor", "kernel": "tc_gemm_kernel<kGroup> (apply+update)",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if achieved else None,

@@ -22,6 +22,7 @@ enum : int {
   kErrWaitAccEmpty = 4,
   kErrWaitSched = 5,
   kErrWaitDrain = 6,
+  kErrWaitDep = 7,
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -77,6 +78,46 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicCAS(err_word, 0, code);
+        return false;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- cross-CTA dependencies
+
+// Release-add to a global counter (after this thread's earlier writes).
+__device__ __forceinline__ void dep_signal(int* counter, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(counter), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int dep_load(const int* counter) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+  return v;
+}
+
+// Order this thread's generic-proxy global accesses with its later (or
+// earlier) async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait until *counter >= target (acquire).  Bounded like mbar_wait: gives up
+// when the CTA's abort flag is raised or after kWaitLimitNs (raising it and
+// recording `code`).
+__device__ __forceinline__ bool dep_wait(const int* counter, int target, volatile int* abort_flag,
+                                         int* err_word, int code) {
+  if (dep_load(counter) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(64);
+    if (dep_load(counter) >= target) return true;
+    if ((i & 63u) == 0) {
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
         *abort_flag = 1;

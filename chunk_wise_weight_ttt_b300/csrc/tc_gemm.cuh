@@ -31,20 +31,31 @@
 //   kDGram   per group of chunks, the same-chunk (block-diagonal) entries of
 //            M_g M_g^T in fp32 for M = Z or M = V (K = the matrix's width);
 //            the update-clipping norms come from these blocks.
-//   kGroup   one group of G chunks: the apply tiles
+//   kGroup   a run of consecutive groups of G chunks of one fast-weight slot,
+//            each group's tiles being its apply tiles
 //              O_g = Z_g W_s^T + S_g V_g            (W_s = state at group start)
-//            and the update tiles
+//            and its update tiles
 //              W <- W_s + V_g^T Z_g,  Wb_next <- bf16(W)
 //            in one launch.  An update tile accumulates V_g^T Z_g from zero
-//            in TMEM; its epilogue adds the fp32 block of W_s in one rounding
-//            (read in a coalesced layout, one 32-column slice ahead, after the
-//            producer prefetched it into L2 at the tile's start) and stores W
-//            and its bf16 copy, coalesced through a per-warp shared-memory
-//            transpose.
+//            in TMEM; its epilogue adds the fp32 block of W_s (or, at a
+//            document start, of W_0) in one rounding (read in a coalesced
+//            layout, one 32-column slice ahead, after the producer prefetched
+//            it into L2 at the tile's start) and stores W and its bf16 copy,
+//            coalesced through a per-warp shared-memory transpose.
 //            Applying W_s to every chunk of the group plus the intra-group
 //            correction S_g V_g equals applying each chunk's own pre-update
 //            state (the deltas are additive, appendix B of the "In-Place
 //            Test-Time Training" summary page).
+//            Groups follow one another inside the launch through completion
+//            counters in global memory, one per (group, 256-row block of W):
+//            an apply tile of group j waits, before it loads W_s, until every
+//            update tile of group j-1 for its rows has stored them; an update
+//            tile of group j waits, before its epilogue touches W, until the
+//            update tiles and the apply tiles of group j-1 for its rows are
+//            done (its stores overwrite what they wrote and what they read).
+//            Tiles are claimed in order and wait only on earlier tiles, so
+//            with every CTA resident the launch cannot deadlock; the waits are
+//            bounded like every other wait of the engine.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -82,12 +93,20 @@ enum GemmMode : int { kSwiGLU = 0, kVProj = 1, kSGram = 2, kGroup = 3, kDGram = 
 //   kVProj:  0 U (64x128), 1 W_target^T (64x128)
 //   kSGram:  0 Z (64x128), 1 Z (64x128)
 //   kDGram:  0 Z or V (64x128), 1 the same (64x128); `f` holds its width
-//   kGroup:  0 Z (64x128), 1 W_s bf16 (64x128), 2 S (64x128),
-//            3 V MN-major (64x64), 4 V MN-major with the group's K extent,
-//            5 Z MN-major (64x64) with the group's K extent,
-//            6 W fp32 of the slot (32 columns x 128 rows)
+//   kGroup:  0 Z (64x128), 1 Wb[0] (64x128), 2 S (64x128),
+//            3 V MN-major (64x64), 4 V MN-major with the run's K extent,
+//            5 Z MN-major (64x64) with the run's K extent,
+//            6 W fp32 of the slot (32 columns x 128 rows), 7 Wb[1] (64x128),
+//            8 W_0 bf16 (64x128)
+constexpr int kNumMaps = 9;
+
+// kGroup per-group flags
+constexpr uint8_t kGrpReset = 1;  // document start: the group's state is W_0
+constexpr uint8_t kGrpInWb1 = 2;  // W_s is in Wb[1] (else Wb[0]; ignored with kGrpReset)
+constexpr uint8_t kGrpOutWb1 = 4; // the update tiles write bf16(W) to Wb[1] (else Wb[0])
+
 struct GemmArgs {
-  CUtensorMap map[7];
+  CUtensorMap map[kNumMaps];
   int n_rows;    // tokens of the call (rows of X/Z/U/V/O)
   int d, f;
   int chunk;
@@ -96,13 +115,21 @@ struct GemmArgs {
   int* err;      // workspace error word
   void* out0;    // kSwiGLU: Z; kVProj: V; kSGram: S; kGroup: O
   void* out1;    // kGroup: W (fp32, updated in place)
-  void* out2;    // kGroup: Wb_next (bf16)
+  void* wb[2];   // kGroup: the two bf16 copies of the state (read / written alternately)
+  const void* w0;  // kGroup: W_0 (bf16)
   // groups
   int s_pad;         // row/column pitch of one S block (multiple of 256)
-  int n_groups;      // kSGram
+  int n_groups;      // groups of the launch (kSGram, kDGram, kGroup)
   int g_start[kMaxGroups];
   int g_len[kMaxGroups];
-  int g0, glen, gslot;  // kGroup
+  // kGroup
+  int g_tile[kMaxGroups + 1];  // first tile pair of each group; [n_groups] = all pairs
+  uint8_t g_flags[kMaxGroups];  // kGrp* bits
+  int slot0;  // S slot of the run's first group (group j uses slot0 + j)
+  // completion counters, zero at launch: [0, n_groups * npd) update tiles,
+  // [n_groups * npd, 2 * n_groups * npd) apply tiles, npd = ceil(d / 256);
+  // each tile pair adds one per epilogue warp of both CTAs
+  int* dep;
   // failure-detection test hook: the leader of the pair that claims tile 0
   // withholds that tile's first ring block, so its bounded waits run out
   int test_withhold_block;
@@ -135,7 +162,20 @@ __device__ __forceinline__ int num_tiles(const GemmArgs& a) {
   if (MODE == kVProj) return cdiv(cdiv(a.n_rows, kBM), 2) * cdiv(a.d, kBN);
   if (MODE == kSGram || MODE == kDGram)
     return a.n_groups * cdiv(cdiv(a.s_pad, kBM), 2) * cdiv(a.s_pad, kBN);
-  return cdiv(cdiv(a.glen, kBM), 2) * cdiv(a.d, kBN) + cdiv(cdiv(a.d, kBM), 2) * cdiv(a.f, kBN);
+  return a.g_tile[a.n_groups];
+}
+
+// Completion-counter targets of one group (kGroup): every tile pair of the
+// 256-row block adds 2 * kEpiWarps.
+__device__ __forceinline__ int upd_target(const GemmArgs& a) { return 2 * kEpiWarps * cdiv(a.f, kBN); }
+__device__ __forceinline__ int app_target(const GemmArgs& a, int g) {
+  return 2 * kEpiWarps * cdiv(cdiv(a.g_len[g], kBM), 2);
+}
+__device__ __forceinline__ int* upd_counter(const GemmArgs& a, int g, int blk) {
+  return a.dep + g * cdiv(a.d, kBN) + blk;
+}
+__device__ __forceinline__ int* app_counter(const GemmArgs& a, int g, int blk) {
+  return a.dep + (a.n_groups + g) * cdiv(a.d, kBN) + blk;
 }
 
 // The tile of pair `t` that CTA `rank` computes.  Everything that decides the
@@ -189,22 +229,30 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int ra
                (c0 / a.chunk <= r1 / a.chunk);
     ti.nkb1 = cdiv(a.f, kBK);
   } else {
-    const int ntA = cdiv(a.d, kBN);
-    const int nA = cdiv(cdiv(a.glen, kBM), 2) * ntA;
-    if (t < nA) {
-      const int mp = t / ntA;
+    // the group of pair t: the last g with g_tile[g] <= t
+    int g = 0;
+#pragma unroll
+    for (int step = kMaxGroups / 2; step > 0; step >>= 1)
+      if (g + step < a.n_groups && a.g_tile[g + step] <= t) g += step;
+    const int len = a.g_len[g], tt = t - a.g_tile[g];
+    const int mpt = cdiv(cdiv(len, kBM), 2);
+    ti.g = g;
+    if (tt < mpt * cdiv(a.d, kBN)) {
+      // apply tiles, column-block major: the first ones need the rows of W_s
+      // that the previous group's first update tiles wrote
+      const int mp = tt % mpt;
       ti.m0 = (2 * mp + rank) * kBM;
-      ti.n0 = (t % ntA) * kBN;
+      ti.n0 = (tt / mpt) * kBN;
       ti.nkb1 = cdiv(a.f, kBK);
       // the correction range of the pair's lower tile; for its upper tile the
       // extra blocks meet S entries that the Gram kernel masked to zero
-      ti.nkb2 = corr_kbound(a.glen, 2 * mp + 1, a.chunk) / kBK;
+      ti.nkb2 = corr_kbound(len, 2 * mp + 1, a.chunk) / kBK;
     } else {
-      const int u = t - nA, ntU = cdiv(a.f, kBN);
+      const int u = tt - mpt * cdiv(a.d, kBN), ntU = cdiv(a.f, kBN);
       ti.kind = 1;
       ti.m0 = (2 * (u / ntU) + rank) * kBM;
       ti.n0 = (u % ntU) * kBN;
-      ti.nkb1 = cdiv(a.glen, kBK);
+      ti.nkb1 = cdiv(len, kBK);
     }
   }
   return ti;
@@ -233,19 +281,25 @@ __device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& t
     tma_load_2d_pair(sa, &a.map[0], bar, kb * kBK, gs + ti.m0);
     tma_load_2d_pair(sb, &a.map[1], bar, kb * kBK, gs + ti.n0 + rank * kh);
   } else {
+    const int gs = a.g_start[ti.g];
     if (ti.kind == 0) {
-      if (kb < ti.nkb1) {
-        tma_load_2d_pair(sa, &a.map[0], bar, kb * kBK, a.g0 + ti.m0);
-        tma_load_2d_pair(sb, &a.map[1], bar, kb * kBK, ti.n0 + rank * kh);
+      // the intra-group correction S_g V_g first (it does not depend on W_s),
+      // then the main product Z_g W_s^T
+      if (kb >= ti.nkb2) {
+        const int k = (kb - ti.nkb2) * kBK;
+        const uint8_t fl = a.g_flags[ti.g];
+        const CUtensorMap* mb = (fl & kGrpReset) ? &a.map[8] : (fl & kGrpInWb1) ? &a.map[7] : &a.map[1];
+        tma_load_2d_pair(sa, &a.map[0], bar, k, gs + ti.m0);
+        tma_load_2d_pair(sb, mb, bar, k, ti.n0 + rank * kh);
       } else {
-        const int k2 = (kb - ti.nkb1) * kBK;
-        tma_load_2d_pair(sa, &a.map[2], bar, k2, a.gslot * a.s_pad + ti.m0);
+        const int k2 = kb * kBK;
+        tma_load_2d_pair(sa, &a.map[2], bar, k2, (a.slot0 + ti.g) * a.s_pad + ti.m0);
 #pragma unroll
         for (int q = 0; q < 2; ++q)
-          tma_load_2d_pair(sb + q * 8192, &a.map[3], bar, ti.n0 + rank * kh + q * 64, a.g0 + k2);
+          tma_load_2d_pair(sb + q * 8192, &a.map[3], bar, ti.n0 + rank * kh + q * 64, gs + k2);
       }
     } else {
-      const int k = a.g0 + kb * kBK;
+      const int k = gs + kb * kBK;
 #pragma unroll
       for (int q = 0; q < kBM / 64; ++q)
         tma_load_2d_pair(sa + q * 8192, &a.map[4], bar, ti.m0 + q * 64, k);
@@ -333,8 +387,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
       // bf16 copy.
       const int lane = row & 31;
       const int rbase = ti.m0 + (row - lane);
+      const uint8_t fl = a.g_flags[ti.g];
+      const bool from_w0 = fl & kGrpReset;
       float* W = reinterpret_cast<float*>(a.out1);
-      __nv_bfloat16* Wb = reinterpret_cast<__nv_bfloat16*>(a.out2);
+      const __nv_bfloat16* W0 = reinterpret_cast<const __nv_bfloat16*>(a.w0);
+      __nv_bfloat16* Wb = reinterpret_cast<__nv_bfloat16*>(a.wb[(fl & kGrpOutWb1) ? 1 : 0]);
       const uint32_t st_row = smem_u32(stg) + lane * 128;
       const int cq = lane & 7;
       float4 wc[8], wn[8];
@@ -343,8 +400,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int wr = rbase + j * 4 + (lane >> 3);
-          dst[j] = (wr < a.d && col < a.f) ? ld_cg_f4(W + (size_t)wr * a.f + col)
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (wr < a.d && col < a.f) {
+            if (from_w0) {
+              const uint2 v = *reinterpret_cast<const uint2*>(W0 + (size_t)wr * a.f + col);
+              const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+              const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+              dst[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            } else {
+              dst[j] = ld_cg_f4(W + (size_t)wr * a.f + col);
+            }
+          } else {
+            dst[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
       };
       load_w(0, wc);
@@ -380,8 +447,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
     } else {
       // plain bf16 store of alpha * acc (kVProj) or acc (kGroup apply)
       const float alpha = (MODE == kVProj) ? a.alpha : 1.0f;
-      const int grow = (MODE == kVProj) ? ti.m0 + row : a.g0 + ti.m0 + row;
-      const bool ok = (MODE == kVProj) ? (grow < a.n_rows) : (ti.m0 + row < a.glen);
+      const int grow = (MODE == kVProj) ? ti.m0 + row : a.g_start[ti.g] + ti.m0 + row;
+      const bool ok = (MODE == kVProj) ? (grow < a.n_rows) : (ti.m0 + row < a.g_len[ti.g]);
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out0) + (size_t)grow * a.d;
 #pragma unroll 1
       for (int s = 0; s < kBN / 32; ++s) {
@@ -516,7 +583,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     if (lane == 0) {
       // ---------------- TMA producer (+ the pair's tile scheduler on the leader)
 #pragma unroll 1
-      for (int q = 0; q < 7; ++q) tma_prefetch_desc(&a.map[q]);
+      for (int q = 0; q < (MODE == kGroup ? kNumMaps : 3); ++q) tma_prefetch_desc(&a.map[q]);
       int stage = 0;
       uint32_t phase = 0;
       int fills = 0;
@@ -541,15 +608,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         if (t >= ntiles) break;
         const TileInfo ti = decode_tile<MODE>(a, t, rank);
         if (!ti.valid) continue;
-        if (MODE == kGroup && ti.kind == 1) {
+        if (MODE == kGroup && ti.kind == 1 && !(a.g_flags[ti.g] & kGrpReset)) {
           // the epilogue adds this tile's fp32 W block after the MMAs; bring
-          // it into L2 now so those reads hit there
+          // it into L2 now so those reads hit there (L2 is the point of
+          // coherence, so a prefetch ahead of the block's last writer is safe)
           for (int b = 0; b < kWBoxes; ++b)
             tma_prefetch_l2_2d(&a.map[6], ti.n0 + b * kWBoxCols, ti.m0);
         }
         const int nkb = ti.nkb1 + ti.nkb2;
 #pragma unroll 1
         for (int kb = 0; kb < nkb; ++kb) {
+          if (MODE == kGroup && ti.kind == 0 && kb == ti.nkb2 && ti.g > 0 &&
+              !(a.g_flags[ti.g] & kGrpReset)) {
+            // W_s rows [n0, n0 + 256) come from the previous group's update
+            // tiles of this launch
+            if (!dep_wait(upd_counter(a, ti.g - 1, ti.n0 / kBN), upd_target(a), abort_flag, a.err,
+                          kErrWaitDep)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_global();  // their generic stores before our TMA reads
+          }
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.err, kErrWaitSmemEmpty)) {
             ok = false;
             break;
@@ -606,19 +685,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         // depends only on the segment is hoisted: a block costs a wait, two
         // ORs, four MMAs with one add each, and a commit.
         constexpr uint64_t kK = sdesc_sw128_hi(0, 1024), kMN = sdesc_sw128_hi(8192, 1024);
+        // apply tiles: correction first, then the main product
+        const bool apply = MODE == kGroup && ti.kind == 0;
+        uint32_t accum = 0u;
 #pragma unroll 1
         for (int seg = 0; seg < 2 && ok; ++seg) {
-          const int cnt = seg == 0 ? ti.nkb1 : ti.nkb2;
+          const int cnt = apply ? (seg == 0 ? ti.nkb2 : ti.nkb1) : (seg == 0 ? ti.nkb1 : 0);
           // operand majors: 0 both K-major, 1 B MN-major (correction),
           // 2 both MN-major (update)
-          const int lay = seg == 1 ? 1 : ((MODE == kGroup && ti.kind == 1) ? 2 : 0);
+          const int lay = apply ? (seg == 0 ? 1 : 0) : ((MODE == kGroup && ti.kind == 1) ? 2 : 0);
           const uint32_t idesc = lay == 0   ? idesc_bf16_f32(2 * kBM, kBN, false, false)
                                  : lay == 1 ? idesc_bf16_f32(2 * kBM, kBN, false, true)
                                             : idesc_bf16_f32(2 * kBM, kBN, true, true);
           const uint64_t ahi = lay == 2 ? kMN : kK, bhi = lay >= 1 ? kMN : kK;
           const uint32_t astep = lay == 2 ? (2048 >> 4) : (32 >> 4);
           const uint32_t bstep = lay >= 1 ? (2048 >> 4) : (32 >> 4);
-          uint32_t accum = seg > 0 ? 1u : 0u;
 #pragma unroll 1
           for (int i = 0; i < cnt; ++i) {
             if (!mbar_wait(&full[stage], phase, abort_flag, a.err, kErrWaitTmaFull)) {
@@ -684,7 +765,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       if (!ok) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + buf * kBN;
+      if (MODE == kGroup && ti.kind == 1 && ti.g > 0) {
+        // this tile rewrites the W block and the bf16 rows that the previous
+        // group's update tiles wrote and its apply tiles read
+        const int blk = ti.m0 / kBN;
+        int okd = dep_wait(upd_counter(a, ti.g - 1, blk), upd_target(a), abort_flag, a.err, kErrWaitDep);
+        if (okd)
+          okd = dep_wait(app_counter(a, ti.g - 1, blk), app_target(a, ti.g - 1), abort_flag, a.err,
+                         kErrWaitDep);
+        if (!__all_sync(0xffffffffu, okd)) break;
+      }
       epilogue_tile<MODE>(a, ti, tacc, row, staging + (warp - 2) * kStgBytesPerWarp);
+      if (MODE == kGroup) {
+        if (ti.kind == 1) {
+          // W and the bf16 copy are stored: make them visible to the next
+          // group's TMA (async-proxy) reads and ordinary reads on other SMs
+          fence_proxy_async_global();
+          __threadfence();
+        }
+        __syncwarp();
+        if (lane == 0)
+          dep_signal(ti.kind == 1 ? upd_counter(a, ti.g, ti.m0 / kBN) : app_counter(a, ti.g, ti.n0 / kBN), 1);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) arrive_leader(&acc_empty[buf]);

@@ -351,12 +351,29 @@ struct PhaseTimer {
   }
 };
 
-int* next_counter(ttt_mlp* h, cudaStream_t st) {
-  if (h->counter_next >= kCtrlInts) {
+// `count` consecutive zeroed ints of the control block for one launch
+// (count <= kCtrlInts - kCounterBase).
+int* next_counters(ttt_mlp* h, cudaStream_t st, int count) {
+  if (h->counter_next + count > kCtrlInts) {
     cudaMemsetAsync(h->ctrl + kCounterBase, 0, (kCtrlInts - kCounterBase) * sizeof(int), st);
     h->counter_next = kCounterBase;
   }
-  return h->ctrl + h->counter_next++;
+  int* p = h->ctrl + h->counter_next;
+  h->counter_next += count;
+  return p;
+}
+
+int* next_counter(ttt_mlp* h, cudaStream_t st) { return next_counters(h, st, 1); }
+
+// Most groups that one group launch chains (TTT_GROUP_RUN overrides, 1..256;
+// 1 gives one launch per group).
+int group_run() {
+  static const int r = [] {
+    const char* v = std::getenv("TTT_GROUP_RUN");
+    const int n = v ? std::atoi(v) : kMaxGroups;
+    return (n >= 1 && n <= kMaxGroups) ? n : kMaxGroups;
+  }();
+  return r;
 }
 
 ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_t n,
@@ -494,17 +511,20 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
       h->prof_launches++;
     }
     pt.begin(4);
-
-    for (size_t i = w0; i < w1; ++i) {
-      const Span& g = groups[i];
-      if (g.reset) {
-        // document start: W <- W_0 (the update tiles accumulate onto W; the
-        // apply tiles read W_0's bf16 values directly)
-        to_f32_kernel<__nv_bfloat16><<<grid_for((long long)wsz, 256), 256, 0, st>>>(
-            (const __nv_bfloat16*)h->w0, W, (long long)wsz);
-        TTT_CK_LAUNCH(h);
-        h->prof_launches++;
-      } else if (h->wb_owner != doc) {
+    // Runs of consecutive groups, one launch each.  A run ends at a group
+    // whose length is not a whole number of K blocks (the update tiles'
+    // operand maps are clipped at its end, so the rows past it read zero).
+    const int npd = cdiv_h(d, kBN);
+    const int run_max = std::min(group_run(), (kCtrlInts - kCounterBase - 1) / (2 * npd));
+    if (run_max < 1) return fail(h, TTT_EINVAL, "d too large for the group launch's counters");
+    auto exact = [&](size_t k) {
+      return groups[k].len % kBK == 0 || (int64_t)groups[k].start + groups[k].len == n;
+    };
+    for (size_t i = w0; i < w1;) {
+      size_t e = i;  // the run's last group
+      while (exact(e) && e + 1 < w1 && (int)(e + 1 - i) < run_max) ++e;
+      if (!groups[i].reset && h->wb_owner != doc) {
+        // the bf16 copy of the state belongs to another slot
         to_bf16_kernel<<<grid_for((long long)wsz, 256), 256, 0, st>>>(W, h->Wb[h->wb_cur], (long long)wsz);
         TTT_CK_LAUNCH(h);
         h->prof_launches++;
@@ -512,34 +532,57 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
       }
       GemmArgs& q = a;
       q.map[0] = map_za;
-      q.map[1] = g.reset ? h->map_w0 : h->map_wb[h->wb_cur];
+      q.map[1] = h->map_wb[0];
       q.map[2] = h->map_s;
       q.map[3] = map_vmn;
       q.map[6] = map_wf;
-      const bool exact = (g.len % kBK == 0) || ((int64_t)g.start + g.len == n);
-      if (exact) {
+      q.map[7] = h->map_wb[1];
+      q.map[8] = h->map_w0;
+      if (exact(e)) {
         q.map[4] = map_vmn;
         q.map[5] = map_zmn;
       } else {
-        const uint64_t ext = (uint64_t)g.start + (uint64_t)g.len;
+        const uint64_t ext = (uint64_t)groups[e].start + (uint64_t)groups[e].len;
         if (!make_map(&q.map[4], h->V, d, ext, d, 64, 64, &why) ||
             !make_map(&q.map[5], h->Z, f, ext, f, 64, 64, &why))
           return fail(h, TTT_ECUDA, why);
       }
+      // per group: its tiles, where its state comes from (W_0 at a document
+      // start, else the bf16 copy the previous group wrote) and where its
+      // update tiles write the next copy
+      q.n_groups = (int)(e - i + 1);
+      int cur = h->wb_cur, tiles = 0;
+      for (int k = 0; k < q.n_groups; ++k) {
+        const Span& g = groups[i + k];
+        q.g_start[k] = g.start;
+        q.g_len[k] = g.len;
+        q.g_tile[k] = tiles;
+        tiles += cdiv_h(cdiv_h(g.len, kBM), 2) * npd + npd * cdiv_h(f, kBN);
+        uint8_t fl = 0;
+        if (g.reset)
+          fl |= kGrpReset;
+        else if (cur)
+          fl |= kGrpInWb1;
+        if (cur ^ 1) fl |= kGrpOutWb1;
+        q.g_flags[k] = fl;
+        cur ^= 1;
+      }
+      q.g_tile[q.n_groups] = tiles;
+      q.slot0 = (int)(i - w0);
       q.out0 = o;
       q.out1 = W;
-      q.out2 = h->Wb[h->wb_cur ^ 1];
-      q.g0 = g.start;
-      q.glen = g.len;
-      q.gslot = (int)(i - w0);
-      q.counter = next_counter(h, st);
-      const int nt = cdiv_h(cdiv_h(g.len, kBM), 2) * cdiv_h(d, kBN) +
-                     cdiv_h(cdiv_h(d, kBM), 2) * cdiv_h(f, kBN);
-      TTT_CK(h, launch_gemm<kGroup>(h, q, nt, st));
+      q.wb[0] = h->Wb[0];
+      q.wb[1] = h->Wb[1];
+      q.w0 = h->w0;
+      int* ctr = next_counters(h, st, 1 + 2 * q.n_groups * npd);
+      q.counter = ctr;
+      q.dep = ctr + 1;
+      TTT_CK(h, launch_gemm<kGroup>(h, q, tiles, st));
       h->prof_launches++;
       h->prof_group_launches++;
-      h->wb_cur ^= 1;
+      h->wb_cur = cur;
       h->wb_owner = doc;
+      i = e + 1;
     }
     pt.end();
   }
