@@ -467,7 +467,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
     // same-chunk entries of the Gram block in fp32, everything else 0
     const int len = a.g_len[ti.g];
     const int i = ti.m0 + row;
-    const int ci = i / a.chunk;
+    // kept: row i in the group, column j in row i's chunk
+    const int jlo = (i / a.chunk) * a.chunk;
+    const int jhi = i < len ? min(len, jlo + a.chunk) : 0;
     float* grow = reinterpret_cast<float*>(a.out0) + ((size_t)ti.g * a.s_pad + i) * a.s_pad;
 #pragma unroll 1
     for (int s = 0; s < kBN / 32; ++s) {
@@ -477,7 +479,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const bool keep = (i < len) && (j0 + j < len) && ((j0 + j) / a.chunk == ci);
+        const bool keep = j0 + j >= jlo && j0 + j < jhi;
         v[j] = keep ? __uint_as_float(r[j]) : 0.0f;
       }
       if (i < a.s_pad) {
@@ -490,7 +492,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
   } else {  // kSGram
     const int len = a.g_len[ti.g];
     const int i = ti.m0 + row;
-    const int ci = i / a.chunk;
+    // kept: row i in the group, column j in a chunk strictly before row i's
+    // (one division per row, none per entry)
+    const int jend = i < len ? min(len, (i / a.chunk) * a.chunk) : 0;
     __nv_bfloat16* srow =
         reinterpret_cast<__nv_bfloat16*>(a.out0) + ((size_t)ti.g * a.s_pad + i) * a.s_pad;
 #pragma unroll 1
@@ -501,9 +505,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
       uint32_t p[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const int ja = j0 + 2 * j, jb = ja + 1;
-        const bool ka = (i < len) && (ja < len) && (ja / a.chunk < ci);
-        const bool kb = (i < len) && (jb < len) && (jb / a.chunk < ci);
+        const int ja = j0 + 2 * j;
+        const bool ka = ja < jend, kb = ja + 1 < jend;
         p[j] = pack_bf16x2(ka ? __uint_as_float(r[2 * j]) : 0.0f,
                            kb ? __uint_as_float(r[2 * j + 1]) : 0.0f);
       }

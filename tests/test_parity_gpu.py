@@ -159,6 +159,57 @@ def test_bf16_tcgen05_ragged_pairs(d, f, T, C, k, starts):
                            torch.from_numpy(np.float32(cfg["w_down0"])))
 
 
+# ------------------------------------------------------------------ chained group launches
+
+# Documents of mixed lengths at d=256, f=512, C=64 (groups of 2048 tokens):
+# twelve groups against six S slots (two waves); runs that end at groups whose
+# length is not a whole number of 64-token K blocks (188, 324, 52 and 204
+# tokens); a document start at every group, so every run has resets inside it.
+CHAIN_STARTS = (0, 256, 512, 700, 1024, 1536, 2048, 2100, 2304, 2560, 3072, 3584)
+
+
+def _chain_cfg():
+    return make_layer(256, 512, 4096, 64, 4, 0.5, dtype="bf16", seed=77, init="qwen",
+                      doc_starts=CHAIN_STARTS)
+
+
+def _chain_run(path=None):
+    """One forward call of the chained-group case; saves (O, W) when `path` is given."""
+    cfg = _chain_cfg()
+    layer, dt = _make_gpu_layer(cfg)
+    o = layer.forward(_dev(cfg["x"], dt), doc_starts=cfg["doc_starts"])
+    w = layer.get_fast_weight()
+    layer.check()
+    res = (o.cpu(), w.cpu())
+    if path:
+        torch.save(res, path)
+    return res
+
+
+def test_chained_groups_waves_runs_and_resets():
+    _check_layer(_chain_cfg(), TOL_BF16, ttt_tol=TOL_TTT_PART, expect_path="tcgen05")
+
+
+@pytest.mark.parametrize("run", ["1", "3"])
+def test_chained_launch_equals_shorter_runs(tmp_path, run):
+    """A tile does the same arithmetic whether its group shares a launch with
+    others or not, so the default launch (every group of a wave chained) must
+    equal runs of at most `run` groups (TTT_GROUP_RUN, read once per process,
+    hence a child process) bit for bit."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = tmp_path / "short_runs.pt"
+    env = dict(os.environ, TTT_GROUP_RUN=run,
+               PYTHONPATH=os.pathsep.join([root, os.path.join(root, "tests")]))
+    subprocess.run([sys.executable, "-c", f"import test_parity_gpu as t; t._chain_run({str(out)!r})"],
+                   env=env, cwd=root, check=True, timeout=600)
+    o_short, w_short = torch.load(out)
+    o_long, w_long = _chain_run()
+    assert torch.equal(o_long, o_short)
+    assert torch.equal(w_long, w_short)
+
+
 # ------------------------------------------------------------------ target windows, clipping
 
 @pytest.mark.parametrize("mode", [1, 2])
