@@ -5,7 +5,10 @@
 // holds rows [128r, 128r+128) of the A block and of the B block (B's N half)
 // in its shared memory, the even CTA issues the MMAs for both, and each CTA's
 // TMEM receives its 128 accumulator rows.  A ring stage is therefore 32 KB per
-// CTA (6 stages) and carries 1.5x the MMA work per byte of a 128x256 tile.
+// CTA and carries 1.5x the MMA work per byte of a 128x256 tile.  The group
+// kernel has 6 stages plus the update tiles' transpose staging; the other
+// modes need no staging and use its space for a seventh stage (the operand
+// stream is latency-bound, so the deeper ring keeps more bytes in flight).
 // The even CTA (the leader) claims tiles from a dynamic counter and hands each
 // to its peer through distributed shared memory; both CTAs' TMA loads signal
 // the leader's ring barriers, and the leader's commits release the stages and
@@ -69,7 +72,6 @@ namespace ttt {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kStages = 6;
 constexpr int kABytes = kBM * kBK * 2;            // 16 KB: this CTA's 128 A rows
 constexpr int kBHalfBytes = (kBN / 2) * kBK * 2;  // 16 KB: this CTA's 128 B rows
 constexpr int kStageBytes = kABytes + kBHalfBytes;  // 32 KB per CTA
@@ -315,7 +317,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// SiLU with the fast-division intrinsic (a few ulp of fp32; the result is
+// rounded to bf16).
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // 16-byte global load cached in L2 only.
 __device__ __forceinline__ float4 ld_cg_f4(const float* p) {
@@ -515,8 +519,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
   }
 }
 
+// Ring depth and dynamic shared memory of each mode.
+template <int MODE>
+__host__ __device__ constexpr int stages_of() {
+  return MODE == kGroup ? 6 : 7;
+}
+template <int MODE>
+__host__ __device__ constexpr int smem_bytes_of() {
+  return 1024 /*align*/ + stages_of<MODE>() * kStageBytes + 1024 /*barriers*/ +
+         (MODE == kGroup ? kEpiWarps * kStgBytesPerWarp : 0);
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ GemmArgs a) {
+  constexpr int kStages = stages_of<MODE>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the dynamic window starts at the same offset in every CTA, so aligning the
   // same way keeps the layout (MMA operand halves, barriers) identical in both
@@ -806,8 +822,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   }
 }
 
-constexpr int kGemmSmemBytes =
-    1024 /*align*/ + kStages * kStageBytes + 1024 /*barriers*/ + kEpiWarps * kStgBytesPerWarp;
-static_assert(kGemmSmemBytes <= 232448, "exceeds the opt-in shared memory of one CTA");
+static_assert(smem_bytes_of<kSwiGLU>() <= 232448 && smem_bytes_of<kGroup>() <= 232448,
+              "exceeds the opt-in shared memory of one CTA");
 
 }  // namespace ttt

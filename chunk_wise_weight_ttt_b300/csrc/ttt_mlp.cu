@@ -282,7 +282,7 @@ cudaError_t launch_pairs(int max_pairs, const GemmArgs& a, int npairs, cudaStrea
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(2 * std::max(1, std::min(max_pairs, npairs)));
   lc.blockDim = dim3(kGemmThreads);
-  lc.dynamicSmemBytes = kGemmSmemBytes;
+  lc.dynamicSmemBytes = smem_bytes_of<MODE>();
   lc.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -307,14 +307,16 @@ cudaError_t setup_tc_kernels(int* max_pairs) {
   const void* kfn[5] = {(const void*)tc_gemm_kernel<kSwiGLU>, (const void*)tc_gemm_kernel<kVProj>,
                         (const void*)tc_gemm_kernel<kSGram>, (const void*)tc_gemm_kernel<kGroup>,
                         (const void*)tc_gemm_kernel<kDGram>};
-  for (const void* k : kfn) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+  const int smem[5] = {smem_bytes_of<kSwiGLU>(), smem_bytes_of<kVProj>(), smem_bytes_of<kSGram>(),
+                       smem_bytes_of<kGroup>(), smem_bytes_of<kDGram>()};
+  for (int i = 0; i < 5; ++i) {
+    cudaError_t e = cudaFuncSetAttribute(kfn[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(2);
   lc.blockDim = dim3(kGemmThreads);
-  lc.dynamicSmemBytes = kGemmSmemBytes;
+  lc.dynamicSmemBytes = smem_bytes_of<kGroup>();
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
