@@ -51,6 +51,16 @@ struct ttt_mlp {
   };
   std::vector<Rec> recs;
   int64_t prof_calls, prof_group_launches, prof_launches;
+  // host-buffer calls: the copy streams and events of the segment pipeline
+  // (created on first use)
+  cudaStream_t st_in = nullptr, st_out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_in = nullptr, ev_out = nullptr;
+  ~ttt_mlp() {
+    for (cudaEvent_t e : {ev_start, ev_in, ev_out})
+      if (e) cudaEventDestroy(e);
+    for (cudaStream_t q : {st_in, st_out})
+      if (q) cudaStreamDestroy(q);
+  }
 };
 
 namespace {
@@ -714,6 +724,32 @@ ttt_status forward_impl(ttt_mlp* h, int doc, const void* x, const void* x0, int6
   return forward_simt_t<float>(h, doc, x, x0, n, spans, o, st);
 }
 
+// Tokens per segment of a host-buffer call (TTT_HOST_SEGMENT overrides it,
+// at least 256).
+int64_t host_segment_tokens() {
+  static const int64_t n = [] {
+    const char* v = std::getenv("TTT_HOST_SEGMENT");
+    const long long t = v ? std::atoll(v) : 4096;
+    return (int64_t)(t >= 256 ? t : 4096);
+  }();
+  return n;
+}
+
+// Where a host-buffer call is cut into segments: at group starts (chunk
+// starts on the fp32 path) at least host_segment_tokens() apart.  A segment
+// that starts at a group start and runs as a call of its own makes the same
+// chunks and groups, and so the same bits, as the whole call: a group start
+// is a chunk start, the conv window never crosses a chunk, and the slot's
+// state carries over.
+std::vector<int64_t> host_cuts(ttt_mlp* h, int64_t n, const int64_t* ds, int nds) {
+  const std::vector<Span> groups = plan_groups(n, h->cfg.chunk, h->tc ? h->G : 1, ds, nds);
+  std::vector<int64_t> cuts{0};
+  for (const Span& g : groups)
+    if (g.start - cuts.back() >= host_segment_tokens()) cuts.push_back(g.start);
+  cuts.push_back(n);
+  return cuts;
+}
+
 ttt_status reset_slot(ttt_mlp* h, int doc, cudaStream_t st) {
   const size_t wsz = (size_t)h->cfg.d * h->cfg.f;
   float* W = h->W + (size_t)doc * wsz;
@@ -857,16 +893,51 @@ ttt_status ttt_mlp_forward_chunks_host(ttt_mlp* h, int32_t doc, const void* x_ho
   ttt_status s = validate_call(h, doc, h->xs, h->x0s, n_tokens, doc_starts, n_doc_starts, h->os);
   if (s != TTT_OK || n_tokens == 0) return s;
   cudaStream_t st = (cudaStream_t)stream;
-  const size_t bytes = (size_t)n_tokens * h->cfg.d * (h->cfg.act_dtype == TTT_BF16 ? 2 : 4);
-  TTT_CK(h, cudaMemcpyAsync(h->xs, x_host, bytes, cudaMemcpyHostToDevice, st));
-  const void* x0d = h->xs;
-  if (x0_host != x_host) {
-    TTT_CK(h, cudaMemcpyAsync(h->x0s, x0_host, bytes, cudaMemcpyHostToDevice, st));
-    x0d = h->x0s;
+  if (!h->st_in) {
+    TTT_CK(h, cudaStreamCreateWithFlags(&h->st_in, cudaStreamNonBlocking));
+    TTT_CK(h, cudaStreamCreateWithFlags(&h->st_out, cudaStreamNonBlocking));
+    for (cudaEvent_t* e : {&h->ev_start, &h->ev_in, &h->ev_out})
+      TTT_CK(h, cudaEventCreateWithFlags(e, cudaEventDisableTiming));
   }
-  s = forward_impl(h, doc, h->xs, x0d, n_tokens, doc_starts, n_doc_starts, h->os, st);
-  if (s != TTT_OK) return s;
-  TTT_CK(h, cudaMemcpyAsync(o_host, h->os, bytes, cudaMemcpyDeviceToHost, st));
+  // Segments pipelined over three streams: segment k+1's input copy (st_in)
+  // and segment k-1's output copy (st_out) overlap segment k's layer on
+  // `stream`.  Events order them; both copy streams first wait for
+  // everything already on `stream` (an earlier call may still read the
+  // staging buffers), and `stream` finally waits for the last output copy.
+  const size_t tok = (size_t)h->cfg.d * (h->cfg.act_dtype == TTT_BF16 ? 2 : 4);
+  const bool sep_x0 = x0_host != x_host;
+  const std::vector<int64_t> cuts = host_cuts(h, n_tokens, doc_starts, n_doc_starts);
+  auto copy_in = [&](size_t k) -> ttt_status {
+    const size_t off = (size_t)cuts[k] * tok, len = (size_t)(cuts[k + 1] - cuts[k]) * tok;
+    TTT_CK(h, cudaMemcpyAsync((char*)h->xs + off, (const char*)x_host + off, len, cudaMemcpyHostToDevice, h->st_in));
+    if (sep_x0)
+      TTT_CK(h, cudaMemcpyAsync((char*)h->x0s + off, (const char*)x0_host + off, len, cudaMemcpyHostToDevice,
+                                h->st_in));
+    TTT_CK(h, cudaEventRecord(h->ev_in, h->st_in));
+    return TTT_OK;
+  };
+  TTT_CK(h, cudaEventRecord(h->ev_start, st));
+  TTT_CK(h, cudaStreamWaitEvent(h->st_in, h->ev_start, 0));
+  TTT_CK(h, cudaStreamWaitEvent(h->st_out, h->ev_start, 0));
+  if ((s = copy_in(0)) != TTT_OK) return s;
+  for (size_t k = 0; k + 1 < cuts.size(); ++k) {
+    const int64_t b = cuts[k], e = cuts[k + 1];
+    TTT_CK(h, cudaStreamWaitEvent(st, h->ev_in, 0));  // input k has landed
+    if (k + 2 < cuts.size() && (s = copy_in(k + 1)) != TTT_OK) return s;
+    std::vector<int64_t> dsk;
+    for (int i = 0; i < n_doc_starts; ++i)
+      if (doc_starts[i] >= b && doc_starts[i] < e) dsk.push_back(doc_starts[i] - b);
+    const size_t off = (size_t)b * tok;
+    s = forward_impl(h, doc, (char*)h->xs + off, (char*)(sep_x0 ? h->x0s : h->xs) + off, e - b, dsk.data(),
+                     (int)dsk.size(), (char*)h->os + off, st);
+    if (s != TTT_OK) return s;
+    TTT_CK(h, cudaEventRecord(h->ev_out, st));
+    TTT_CK(h, cudaStreamWaitEvent(h->st_out, h->ev_out, 0));
+    TTT_CK(h, cudaMemcpyAsync((char*)o_host + off, (char*)h->os + off, (size_t)(e - b) * tok,
+                              cudaMemcpyDeviceToHost, h->st_out));
+  }
+  TTT_CK(h, cudaEventRecord(h->ev_out, h->st_out));
+  TTT_CK(h, cudaStreamWaitEvent(st, h->ev_out, 0));
   return TTT_OK;
 }
 

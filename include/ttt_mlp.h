@@ -128,8 +128,14 @@ ttt_status ttt_mlp_forward_chunks(ttt_mlp* h, int32_t doc, const void* x, const 
 
 /* The same call with host buffers: x_host / x0_host are copied to device
  * staging inside the workspace, the layer runs, and O is copied back into
- * o_host, all on `stream`.  Pinned (page-locked) host buffers make the copies
- * asynchronous; the call returns once they are enqueued, so the caller must
+ * o_host.  The call is cut at group starts into segments of about 4096 tokens
+ * (TTT_HOST_SEGMENT overrides), which give the same bits as one call; segment
+ * k+1's input copy and segment k-1's output copy run on two copy streams of
+ * the handle while segment k runs on `stream`.  The copies start after
+ * everything already enqueued on `stream`, and `stream` waits for the last
+ * one, so stream order is as if everything ran on `stream`.  Pinned
+ * (page-locked) host buffers make the copies asynchronous and let them
+ * overlap; the call returns once everything is enqueued, so the caller must
  * synchronise `stream` before reading o_host or reusing x_host. */
 ttt_status ttt_mlp_forward_chunks_host(ttt_mlp* h, int32_t doc, const void* x_host,
                                        const void* x0_host, int64_t n_tokens,

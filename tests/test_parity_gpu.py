@@ -364,6 +364,29 @@ def test_host_buffer_entry_point():
     assert _rel(_host(oh), o_ref) < TOL_BF16
 
 
+def test_host_buffer_segments_equal_device_call():
+    """A host-buffer call cut into five segments (at 9000, a document start,
+    and at 4096, 13096 and 19049, group starts inside documents), with an X0
+    that differs from X, equals the device-buffer call bit for bit, output and
+    final state."""
+    cfg = make_layer(256, 512, 20000, 64, 4, 0.5, dtype="bf16", seed=5, init="qwen",
+                     doc_starts=(0, 5000, 9000, 17001))
+    dt = torch.bfloat16
+    x = _dev(cfg["x"], dt)
+    x0 = (x.float() * 0.5 + 0.01).to(dt)
+    dev_layer, _ = _make_gpu_layer(cfg)
+    o_dev = dev_layer.forward(x, x0, doc_starts=cfg["doc_starts"])
+    w_dev = dev_layer.get_fast_weight()
+    dev_layer.check()
+    host_layer, _ = _make_gpu_layer(cfg)
+    xh, x0h = x.cpu().pin_memory(), x0.cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    host_layer.forward_host(xh, x0h, out_host=oh, doc_starts=cfg["doc_starts"])
+    host_layer.check()
+    assert torch.equal(oh, o_dev.cpu())
+    assert torch.equal(host_layer.get_fast_weight(), w_dev)
+
+
 def test_bad_call_arguments_change_nothing():
     from chunk_wise_weight_ttt_b300 import TTTError
     cfg = _bf16_cfg(T=256, C=64)
