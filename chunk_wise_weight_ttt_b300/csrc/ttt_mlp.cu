@@ -736,16 +736,19 @@ int64_t host_segment_tokens() {
 }
 
 // Where a host-buffer call is cut into segments: at group starts (chunk
-// starts on the fp32 path) at least host_segment_tokens() apart.  A segment
-// that starts at a group start and runs as a call of its own makes the same
-// chunks and groups, and so the same bits, as the whole call: a group start
-// is a chunk start, the conv window never crosses a chunk, and the slot's
-// state carries over.
+// starts on the fp32 path), the first segment at least half of
+// host_segment_tokens() long and the others at least host_segment_tokens()
+// (the first segment's input copy cannot overlap a layer, so it is kept
+// short).  A segment that starts at a group start and runs as a call of its
+// own makes the same chunks and groups, and so the same bits, as the whole
+// call: a group start is a chunk start, the conv window never crosses a
+// chunk, and the slot's state carries over.
 std::vector<int64_t> host_cuts(ttt_mlp* h, int64_t n, const int64_t* ds, int nds) {
   const std::vector<Span> groups = plan_groups(n, h->cfg.chunk, h->tc ? h->G : 1, ds, nds);
   std::vector<int64_t> cuts{0};
   for (const Span& g : groups)
-    if (g.start - cuts.back() >= host_segment_tokens()) cuts.push_back(g.start);
+    if (g.start - cuts.back() >= (cuts.size() == 1 ? host_segment_tokens() / 2 : host_segment_tokens()))
+      cuts.push_back(g.start);
   cuts.push_back(n);
   return cuts;
 }
