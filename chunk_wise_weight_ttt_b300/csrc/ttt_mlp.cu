@@ -985,8 +985,12 @@ ttt_status ttt_mlp_check(ttt_mlp* h, void* stream) {
   TTT_CK(h, cudaMemcpy(&word, h->ctrl, sizeof(int), cudaMemcpyDeviceToHost));
   if (word != 0) {
     TTT_CK(h, cudaMemset(h->ctrl, 0, sizeof(int)));
-    char buf[96];
-    std::snprintf(buf, sizeof buf, "an in-kernel wait ran out (code %d)", word);
+    static const char* const kWaitNames[] = {"?", "operand stage full", "operand stage empty",
+                                             "accumulator full", "accumulator empty",
+                                             "tile scheduler", "drain", "completion counter"};
+    char buf[128];
+    std::snprintf(buf, sizeof buf, "an in-kernel wait ran out (code %d: %s)", word,
+                  kWaitNames[(word >= 1 && word <= 7) ? word : 0]);
     return fail(h, TTT_ETIMEOUT, buf);
   }
   return TTT_OK;
