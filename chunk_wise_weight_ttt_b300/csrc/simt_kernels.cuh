@@ -49,6 +49,8 @@ __device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
   *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
   *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
 }
+__device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_float(float v) { return v; }
 
 // Token spans whose chunking is regular: span i covers [start[i], start[i] +
 // len[i]) and its chunks are [start + c*chunk, ...) clipped to the span end.
@@ -66,8 +68,10 @@ struct SpanList {
 // kConvCh channels of the tokens covered by `spans`: it stages the X0 rows
 // those tokens read (tokens + k - 1 rows) in shared memory with asynchronous
 // 16-byte copies (all in flight at once; zero-filled outside the spans), so
-// every row comes from HBM once, then each thread computes 8 channels of
-// tokens / 8 tokens.  Tokens outside every span are untouched.
+// every row comes from HBM once, and its channels' tap weights as fp32; then
+// each thread computes 8 channels of a run of tokens / 8 consecutive tokens,
+// finding its span and chunk once and stepping them along the run.  Tokens
+// outside every span are untouched.
 // Grid: (ceil(span tokens / conv_tokens<TIn>()), ceil(d / kConvCh)).
 constexpr int kConvCh = 256;
 template <typename TIn>
@@ -89,6 +93,7 @@ __global__ void __launch_bounds__(256) conv_target_kernel(const TIn* __restrict_
   constexpr int kConvTok = conv_tokens<TIn>();
   constexpr int kConvRows = kConvTok + 8;  // k <= 8
   __shared__ __align__(16) TIn slab[kConvRows * kConvCh];
+  __shared__ __align__(16) float wsm[8 * kConvCh];  // tap j, channel c at j * kConvCh + c
   const int first = spans.start[0];
   const int last = spans.start[spans.n - 1] + spans.len[spans.n - 1];  // exclusive
   const int t0 = first + blockIdx.x * kConvTok;
@@ -106,6 +111,10 @@ __global__ void __launch_bounds__(256) conv_target_kernel(const TIn* __restrict_
     cp_async16(slab + r * kConvCh + cg * 8 + pc * (16 / (int)sizeof(TIn)),
                reinterpret_cast<const uint8_t*>(src) + pc * 16, in ? 16 : 0);
   }
+  for (int q = threadIdx.x; q < k * kConvCh; q += blockDim.x) {
+    const int j = q / kConvCh, c = ch0 + q % kConvCh;
+    wsm[q] = c < d ? to_float(conv_w[(size_t)j * d + c]) : 0.0f;
+  }
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   const int cg = threadIdx.x % kChunks, tl = threadIdx.x / kChunks;
@@ -113,18 +122,29 @@ __global__ void __launch_bounds__(256) conv_target_kernel(const TIn* __restrict_
   if (ch >= d) return;
   const int base = (mode == 1) ? 0 : 1;
   const int step = (mode == 2) ? -1 : 1;
-  for (int i = tl; i < kConvTok; i += 256 / kChunks) {
-    const int t = t0 + i;
+  constexpr int kRun = kConvTok / (256 / kChunks);  // consecutive tokens per thread
+  int s_end = -1, cbeg = 0, cend = 0;               // current span end and chunk
+  for (int i = 0; i < kRun; ++i) {
+    const int t = t0 + tl * kRun + i;
     if (t >= last) break;
-    int lo = 0, hi = spans.n - 1;
-    while (lo < hi) {  // last span starting at or before t
-      const int mid = (lo + hi + 1) / 2;
-      if (spans.start[mid] <= t) lo = mid; else hi = mid - 1;
+    if (t >= s_end) {
+      int lo = 0, hi = spans.n - 1;
+      while (lo < hi) {  // last span starting at or before t
+        const int mid = (lo + hi + 1) / 2;
+        if (spans.start[mid] <= t) lo = mid; else hi = mid - 1;
+      }
+      const int s0 = spans.start[lo];
+      s_end = s0 + spans.len[lo];
+      if (t >= s_end) {  // in a gap between spans
+        s_end = -1;
+        continue;
+      }
+      cbeg = s0 + ((t - s0) / spans.chunk) * spans.chunk;
+      cend = min(cbeg + spans.chunk, s_end);
+    } else if (t >= cend) {  // the next chunk of the span
+      cbeg = cend;
+      cend = min(cbeg + spans.chunk, s_end);
     }
-    const int s0 = spans.start[lo];
-    if (t >= s0 + spans.len[lo]) continue;  // in a gap between spans
-    const int cbeg = s0 + ((t - s0) / spans.chunk) * spans.chunk;
-    const int cend = min(cbeg + spans.chunk, s0 + spans.len[lo]);
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
@@ -132,9 +152,11 @@ __global__ void __launch_bounds__(256) conv_target_kernel(const TIn* __restrict_
     for (int j = 0; j < 8; ++j) {
       const int src = t + base + step * j;
       if (j < k && src >= cbeg && src < cend) {
-        float xv[8], wv[8];
+        float xv[8];
         load8(slab + (src - t0 - omin) * kConvCh + cg * 8, xv);
-        load8(conv_w + (size_t)j * d + ch, wv);  // L1-resident: k x 16 bytes per thread
+        const float4 w0 = *reinterpret_cast<const float4*>(wsm + j * kConvCh + cg * 8);
+        const float4 w1 = *reinterpret_cast<const float4*>(wsm + j * kConvCh + cg * 8 + 4);
+        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = fmaf(wv[e], xv[e], acc[e]);
       }
