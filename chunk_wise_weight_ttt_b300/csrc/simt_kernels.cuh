@@ -49,8 +49,6 @@ __device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
   *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
   *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
 }
-__device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
-__device__ __forceinline__ float to_float(float v) { return v; }
 
 // Token spans whose chunking is regular: span i covers [start[i], start[i] +
 // len[i]) and its chunks are [start + c*chunk, ...) clipped to the span end.
@@ -66,12 +64,14 @@ struct SpanList {
 // window), j (current-token window) or 1 - j (causal window), by `mode`.
 // A CTA (256 threads) computes conv_tokens<TIn>() consecutive tokens x
 // kConvCh channels of the tokens covered by `spans`: it stages the X0 rows
-// those tokens read (tokens + k - 1 rows) in shared memory with asynchronous
+// those tokens read (tokens + KT - 1 rows) in shared memory with asynchronous
 // 16-byte copies (all in flight at once; zero-filled outside the spans), so
-// every row comes from HBM once, and its channels' tap weights as fp32; then
-// each thread computes 8 channels of a run of tokens / 8 consecutive tokens,
-// finding its span and chunk once and stepping them along the run.  Tokens
-// outside every span are untouched.
+// every row comes from HBM once.  A thread then owns 4 channels and a run of
+// consecutive tokens: it keeps its KT tap weights and a window of the last KT
+// rows in registers and slides the window one row per token, so shared
+// memory delivers each row to it once rather than once per tap (the per-tap
+// form was bound by shared-memory bandwidth).  Tokens outside every span are
+// untouched.  KT = k, the number of taps (1..8).
 // Grid: (ceil(span tokens / conv_tokens<TIn>()), ceil(d / kConvCh)).
 constexpr int kConvCh = 256;
 template <typename TIn>
@@ -85,24 +85,43 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src,
                : "memory");
 }
 
-template <typename TIn, typename TOut>
-__global__ void __launch_bounds__(256) conv_target_kernel(const TIn* __restrict__ x0,
+// 4 consecutive elements (8-byte aligned for bf16, 16-byte for fp32) as floats.
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 q = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.y));
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* p, const float (&v)[4]) {
+  uint2 q;
+  *reinterpret_cast<__nv_bfloat162*>(&q.x) = __floats2bfloat162_rn(v[0], v[1]);
+  *reinterpret_cast<__nv_bfloat162*>(&q.y) = __floats2bfloat162_rn(v[2], v[3]);
+  *reinterpret_cast<uint2*>(p) = q;
+}
+__device__ __forceinline__ void store4(float* p, const float (&v)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+
+template <typename TIn, typename TOut, int KT>
+__global__ void __launch_bounds__(256, 2) conv_target_kernel(const TIn* __restrict__ x0,
                                                           const TIn* __restrict__ conv_w,
-                                                          TOut* __restrict__ u, int d, int k,
+                                                          TOut* __restrict__ u, int d,
                                                           const SpanList spans, int mode) {
   constexpr int kConvTok = conv_tokens<TIn>();
-  constexpr int kConvRows = kConvTok + 8;  // k <= 8
-  __shared__ __align__(16) TIn slab[kConvRows * kConvCh];
-  __shared__ __align__(16) float wsm[8 * kConvCh];  // tap j, channel c at j * kConvCh + c
+  constexpr int kRows = kConvTok + KT - 1;  // X0 rows the CTA's tokens read
+  __shared__ __align__(16) TIn slab[kRows * kConvCh];
   const int first = spans.start[0];
   const int last = spans.start[spans.n - 1] + spans.len[spans.n - 1];  // exclusive
   const int t0 = first + blockIdx.x * kConvTok;
   const int ch0 = blockIdx.y * kConvCh;
-  const int omin = (mode == 2) ? 2 - k : (mode == 1 ? 0 : 1);  // smallest tap offset
-  const int nrows = kConvTok + k - 1;
+  const int omin = (mode == 2) ? 2 - KT : (mode == 1 ? 0 : 1);  // smallest tap offset
   constexpr int kChunks = kConvCh / 8;                 // groups of 8 channels per row
   constexpr int kPieces = 8 * (int)sizeof(TIn) / 16;   // 16-byte copies per group
-  for (int q = threadIdx.x; q < nrows * kChunks * kPieces; q += blockDim.x) {
+  for (int q = threadIdx.x; q < kRows * kChunks * kPieces; q += blockDim.x) {
     const int pc = q % kPieces, rc = q / kPieces;
     const int r = rc / kChunks, cg = rc % kChunks;
     const int row = t0 + omin + r, ch = ch0 + cg * 8;
@@ -111,22 +130,35 @@ __global__ void __launch_bounds__(256) conv_target_kernel(const TIn* __restrict_
     cp_async16(slab + r * kConvCh + cg * 8 + pc * (16 / (int)sizeof(TIn)),
                reinterpret_cast<const uint8_t*>(src) + pc * 16, in ? 16 : 0);
   }
-  for (int q = threadIdx.x; q < k * kConvCh; q += blockDim.x) {
-    const int j = q / kConvCh, c = ch0 + q % kConvCh;
-    wsm[q] = c < d ? to_float(conv_w[(size_t)j * d + c]) : 0.0f;
+  constexpr int kQuads = kConvCh / 4;     // threads per token lane (4 channels each)
+  constexpr int kLanes = 256 / kQuads;    // token lanes
+  constexpr int kRun = kConvTok / kLanes; // consecutive tokens per thread
+  const int cq = threadIdx.x % kQuads, tl = threadIdx.x / kQuads;
+  const int ch = ch0 + cq * 4;
+  // window slot s holds row t + omin + s; its tap is j = s, or KT - 1 - s for
+  // the causal window (off(j) = 1 - j)
+  float w[KT][4];
+  if (ch < d) {
+#pragma unroll
+    for (int s = 0; s < KT; ++s) load4(conv_w + (size_t)(mode == 2 ? KT - 1 - s : s) * d + ch, w[s]);
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  const int cg = threadIdx.x % kChunks, tl = threadIdx.x / kChunks;
-  const int ch = ch0 + cg * 8;
   if (ch >= d) return;
-  const int base = (mode == 1) ? 0 : 1;
-  const int step = (mode == 2) ? -1 : 1;
-  constexpr int kRun = kConvTok / (256 / kChunks);  // consecutive tokens per thread
-  int s_end = -1, cbeg = 0, cend = 0;               // current span end and chunk
+  const int r0 = tl * kRun;  // slab row of slot 0 for the thread's first token
+  float win[KT][4];
+#pragma unroll
+  for (int s = 1; s < KT; ++s) load4(slab + (r0 + s - 1) * kConvCh + cq * 4, win[s]);
+  int s_end = -1, cbeg = 0, cend = 0;  // current span end and chunk
+#pragma unroll
   for (int i = 0; i < kRun; ++i) {
-    const int t = t0 + tl * kRun + i;
-    if (t >= last) break;
+#pragma unroll
+    for (int s = 0; s + 1 < KT; ++s)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) win[s][c] = win[s + 1][c];
+    load4(slab + (r0 + i + KT - 1) * kConvCh + cq * 4, win[KT - 1]);
+    const int t = t0 + r0 + i;
+    if (t >= last) continue;
     if (t >= s_end) {
       int lo = 0, hi = spans.n - 1;
       while (lo < hi) {  // last span starting at or before t
@@ -145,24 +177,31 @@ __global__ void __launch_bounds__(256) conv_target_kernel(const TIn* __restrict_
       cbeg = cend;
       cend = min(cbeg + spans.chunk, s_end);
     }
-    float acc[8];
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+    for (int s = 0; s < KT; ++s) {
+      const int r = t + omin + s;
+      if (r >= cbeg && r < cend) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int src = t + base + step * j;
-      if (j < k && src >= cbeg && src < cend) {
-        float xv[8];
-        load8(slab + (src - t0 - omin) * kConvCh + cg * 8, xv);
-        const float4 w0 = *reinterpret_cast<const float4*>(wsm + j * kConvCh + cg * 8);
-        const float4 w1 = *reinterpret_cast<const float4*>(wsm + j * kConvCh + cg * 8 + 4);
-        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = fmaf(wv[e], xv[e], acc[e]);
+        for (int c = 0; c < 4; ++c) acc[c] = fmaf(w[s][c], win[s][c], acc[c]);
       }
     }
-    store8(u + (size_t)t * d + ch, acc);
+    store4(u + (size_t)t * d + ch, acc);
   }
+}
+
+// Launch conv_target_kernel for k taps (1..8) on `st`.
+template <typename TIn, typename TOut>
+inline cudaError_t launch_conv(dim3 grid, cudaStream_t st, const TIn* x0, const TIn* conv_w, TOut* u,
+                               int d, int k, const SpanList& spans, int mode) {
+  using Fn = void (*)(const TIn*, const TIn*, TOut*, int, const SpanList, int);
+  const Fn fns[8] = {conv_target_kernel<TIn, TOut, 1>, conv_target_kernel<TIn, TOut, 2>,
+                     conv_target_kernel<TIn, TOut, 3>, conv_target_kernel<TIn, TOut, 4>,
+                     conv_target_kernel<TIn, TOut, 5>, conv_target_kernel<TIn, TOut, 6>,
+                     conv_target_kernel<TIn, TOut, 7>, conv_target_kernel<TIn, TOut, 8>};
+  if (k < 1 || k > 8) return cudaErrorInvalidValue;
+  fns[k - 1]<<<grid, 256, 0, st>>>(x0, conv_w, u, d, spans, mode);
+  return cudaGetLastError();
 }
 
 // C(m,n) = alpha * sum_k A(m,k) B(k,n) + beta * C(m,n), fp32 accumulation.

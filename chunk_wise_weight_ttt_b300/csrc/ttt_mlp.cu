@@ -230,7 +230,7 @@ ttt_status fail(ttt_mlp* h, ttt_status s, const std::string& msg) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Launch shape of conv_target_kernel<TIn, .> for the tokens the span list covers.
+// Launch shape of conv_target_kernel<TIn, ., .> for the tokens the span list covers.
 template <typename TIn>
 dim3 conv_grid(const SpanList& sl, int d) {
   const int ntok = sl.start[sl.n - 1] + sl.len[sl.n - 1] - sl.start[0];
@@ -420,10 +420,9 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
       sl.start[i - w0] = groups[i].start;
       sl.len[i - w0] = groups[i].len;
     }
-    conv_target_kernel<__nv_bfloat16, __nv_bfloat16><<<conv_grid<__nv_bfloat16>(sl, d), 256, 0, st>>>(
-        (const __nv_bfloat16*)x0, (const __nv_bfloat16*)h->conv, (__nv_bfloat16*)h->U, d, c.conv_k, sl,
-        c.target_mode);
-    TTT_CK_LAUNCH(h);
+    TTT_CK(h, launch_conv(conv_grid<__nv_bfloat16>(sl, d), st, (const __nv_bfloat16*)x0,
+                          (const __nv_bfloat16*)h->conv, (__nv_bfloat16*)h->U, d, c.conv_k, sl,
+                          c.target_mode));
     h->prof_launches++;
   }
   pt.end();
@@ -630,9 +629,7 @@ ttt_status forward_simt_t(ttt_mlp* h, int doc, const void* xv, const void* x0v, 
       sl.start[i - w0] = spans[i].start;
       sl.len[i - w0] = spans[i].len;
     }
-    conv_target_kernel<T, float><<<conv_grid<T>(sl, d), 256, 0, st>>>(x0, (const T*)h->conv, U, d, c.conv_k, sl,
-                                                                     c.target_mode);
-    TTT_CK_LAUNCH(h);
+    TTT_CK(h, launch_conv(conv_grid<T>(sl, d), st, x0, (const T*)h->conv, U, d, c.conv_k, sl, c.target_mode));
     h->prof_launches++;
   }
   dim3 gv((d + 63) / 64, (nn + 63) / 64);
@@ -1169,9 +1166,8 @@ extern "C" ttt_status ttt_target_noalloc(const void* x0, const void* conv_w, con
       sl.start[i - w0] = docs[i].start;
       sl.len[i - w0] = docs[i].len;
     }
-    conv_target_kernel<__nv_bfloat16, __nv_bfloat16><<<conv_grid<__nv_bfloat16>(sl, d), 256, 0, st>>>(
-        (const __nv_bfloat16*)x0, (const __nv_bfloat16*)conv_w, u, d, conv_k, sl, /*mode=*/0);
-    TTT_CK(nullptr, cudaGetLastError());
+    TTT_CK(nullptr, launch_conv(conv_grid<__nv_bfloat16>(sl, d), st, (const __nv_bfloat16*)x0,
+                                (const __nv_bfloat16*)conv_w, u, d, conv_k, sl, /*mode=*/0));
   }
 
   std::string why;
