@@ -278,6 +278,20 @@ def test_eta_zero_is_static_mlp():
     assert np.array_equal(w, np.float64(cfg["w_down0"]))
 
 
+@pytest.mark.parametrize("zeroed", ["conv_w", "w_target"])
+def test_zero_target_is_static_mlp(zeroed):
+    """A zero conv or a zero target projection makes every V zero ("In-Place
+    Test-Time Training" summary page, section 3, LM-Aligned Objective: the
+    target is Conv1D(X0) W_target): the layer is the static MLP for any eta and
+    W stays W_0 exactly."""
+    cfg = _tiny(d=8, f=24, T=40, C=8, k=3)
+    cfg = {**cfg, zeroed: np.zeros_like(cfg[zeroed])}
+    o, w = _run(cfg, eta=0.5)
+    ref = _torch_static_mlp(cfg["x"], cfg["w_gate"], cfg["w_up"], cfg["w_down0"])
+    assert _rel(o, ref) < 1e-14
+    assert np.array_equal(w, np.float64(cfg["w_down0"]))
+
+
 def test_single_chunk_apply_before_update():
     """T <= C: the output is the static MLP for any eta; W_final = W_0 + eta V^T Z."""
     cfg = _tiny(d=8, f=24, T=10, C=16, k=3, eta=5.0)
