@@ -310,6 +310,21 @@ def test_eta_zero_keeps_w0_bitwise():
     assert np.array_equal(_host(w), np.float64(cfg["w_down0"]))
 
 
+def test_zero_conv_keeps_w0_bitwise_for_any_eta():
+    """With a zero conv every target is zero, so every update adds exact zeros:
+    W stays W_0 bit for bit on the tcgen05 path, and O is the static MLP."""
+    cfg = _bf16_cfg(T=1100, C=64, eta=0.5)
+    cfg = {**cfg, "conv_w": np.zeros_like(cfg["conv_w"])}
+    layer, dt = _make_gpu_layer(cfg)
+    assert layer.path == "tcgen05"
+    o = layer.forward(_dev(cfg["x"], dt))
+    w = layer.get_fast_weight()
+    layer.check()
+    assert np.array_equal(_host(w), np.float64(cfg["w_down0"]))
+    o_ref, _ = _oracle(cfg, eta=0.0)
+    assert _rel(_host(o), o_ref) < TOL_BF16
+
+
 def test_state_persists_across_calls_and_reset():
     """Two calls (the second continues the document) equal the oracle run from
     the first call's final state; reset() restores W_0 exactly."""
