@@ -136,7 +136,10 @@ ttt_status ttt_mlp_forward_chunks(ttt_mlp* h, int32_t doc, const void* x, const 
  * one, so stream order is as if everything ran on `stream`.  Pinned
  * (page-locked) host buffers make the copies asynchronous and let them
  * overlap; the call returns once everything is enqueued, so the caller must
- * synchronise `stream` before reading o_host or reusing x_host. */
+ * synchronise `stream` before reading o_host or reusing x_host.  If the call
+ * fails after its first segment was enqueued, copies of earlier segments may
+ * still be in flight on the copy streams: synchronise the device before
+ * freeing or reusing the host buffers. */
 ttt_status ttt_mlp_forward_chunks_host(ttt_mlp* h, int32_t doc, const void* x_host,
                                        const void* x0_host, int64_t n_tokens,
                                        const int64_t* doc_starts, int32_t n_doc_starts,
