@@ -1,7 +1,8 @@
 // Inline-PTX building blocks for sm_100-family (sm_103a) kernels: mbarriers
-// (local and across a CTA pair of a cluster), TMA tensor loads (plain and
-// multicast), and the 5th-generation tensor core (tcgen05: TMEM allocation,
-// MMA issue, smem->TMEM copy, commit, TMEM loads).  Every mbarrier wait here is
+// (local and across a CTA pair of a cluster), TMA tensor loads into one CTA's
+// own shared memory (no multicast loads) and L2 prefetches, and the
+// 5th-generation tensor core in its CTA-pair form (tcgen05 cta_group::2: TMEM
+// allocation, MMA issue, commit, TMEM loads).  Every mbarrier wait here is
 // bounded by wall-clock time so that no kernel can hang the GPU.
 #pragma once
 
@@ -179,29 +180,6 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 2-D tiled load of one box into shared memory; completion is signalled on
-// `bar` as transaction bytes.  c0 is the innermost coordinate (elements).
-__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
-                                            int32_t c0, int32_t c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// The same box written to the same shared-memory offset of every CTA in
-// `cta_mask`; each destination CTA's mbarrier at `bar`'s offset receives the
-// box's transaction bytes.
-__device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
-                                               int32_t c0, int32_t c1, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask)
-      : "memory");
-}
-
 // Load of one box into this CTA's shared memory whose completion (transaction
 // bytes) is signalled on an mbarrier that may lie in the peer CTA of a CTA pair
 // (`bar_cluster` is a shared::cluster address, e.g. from cluster_map).
@@ -225,25 +203,8 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32
 
 // ---------------------------------------------------------------- tcgen05
 //
-// Kernels that pair two CTAs on one MMA use the cta_group::2 forms below for
-// every tcgen05 instruction (allocation, MMA, copy, commit); the two groups
-// are never mixed within one kernel.
-
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(dst_smem)),
-               "r"(ncols)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
+// The engine pairs two CTAs on one MMA, so every tcgen05 instruction here is
+// the cta_group::2 form (allocation, MMA, commit).
 
 // cta_group::2: one warp of each CTA of the pair performs these together; the
 // same columns are allocated in both CTAs' TMEM.
@@ -269,17 +230,6 @@ __device__ __forceinline__ void tc_fence_before() {
 
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// D(tmem, fp32) (+)= A(smem desc) * B(smem desc), bf16 operands; one thread issues.
-__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
 }
 
 // Pair MMA (cta_group::2), issued by one thread of the even CTA: A rows
@@ -315,24 +265,6 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint64_t* bar, uint16_t cta_ma
 }
 
 
-// Arrive (once) on `bar` when every tcgen05 op issued so far by this thread is done.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// As tc_commit, but the arrival goes to the mbarrier at `bar`'s offset in every
-// CTA of `cta_mask`.
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
 // Field layout: [4,6) D format (1 = f32), [7,10) A format (1 = bf16),
 // [10,13) B format (1 = bf16), bit 15 A major (1 = MN-major), bit 16 B major,
@@ -350,18 +282,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
 //   lbo unused, sbo = 1024.
 // MN-major operand (rows of 128 B = 64 bf16 along M/N, one row per K index,
 //   64-element M/N blocks `lbo` bytes apart, 8-row K groups `sbo` = 1024 apart).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16;
-  d |= static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32;
-  d |= 1ull << 46;
-  d |= 2ull << 61;
-  return d;
-}
-
-// The constant (address-free) part of sdesc_sw128(., lbo, sbo): a descriptor
-// for shared-memory address `a` is this value | ((a & 0x3FFFF) >> 4), and
+// The constant (address-free) part of such a descriptor: the descriptor for
+// shared-memory address `a` is this value | ((a & 0x3FFFF) >> 4), and
 // advancing the address by `off` bytes adds off >> 4 (the operands lie below
 // 2^18, so the 14-bit start field never carries).
 __host__ __device__ constexpr uint64_t sdesc_sw128_hi(uint32_t lbo, uint32_t sbo) {
