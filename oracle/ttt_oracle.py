@@ -57,6 +57,7 @@ __all__ = [
     "chunk_delta_norms",
     "chunk_spans",
     "ttt_layer",
+    "ttt_core",
     "ttt_layer_rows",
     "rms_norm",
     "ttt_stack",
@@ -187,6 +188,31 @@ def ttt_layer(x, x0, w_gate, w_up, w_down0, conv_w, w_target, eta, chunk,
         out[s:e] = z @ W.T
         v = chunk_target(x0[s:e], conv_w, w_target, target_mode)
         W = W + clip_delta(float(eta) * (v.T @ z), clip_tau)
+    return out, W
+
+
+def ttt_core(z, v, w_down0, eta, chunk, doc_starts=(0,), w_init=None):
+    """The chunk recursion alone, given the per-token intermediates.
+
+    For every chunk c in order ([BLOG] 3 "apply then update"):
+      O_c = Z_c W_c^T                      (the state before this chunk's update)
+      W_{c+1} = W_c + eta V_c^T Z_c        ([BLOG] 2, 4)
+    with W starting at ``w_init`` (default W_0) and reset to W_0 at each
+    document start ([SUM] B).  ``z`` (n x f) is the gated intermediate and
+    ``v`` (n x d) the target, each row computed for the chunk that holds it
+    (the target is chunk-local, reading R1).  This is the apply+update part of
+    ttt_layer without the producers; no clipping.  Returns (O n x d, final W)."""
+    z = _f64(z)
+    v = _f64(v)
+    w0 = _f64(w_down0)
+    n = z.shape[0]
+    W = w0.copy() if w_init is None else _f64(w_init).copy()
+    out = np.zeros((n, w0.shape[0]), dtype=np.float64)
+    for s, e, reset in chunk_spans(n, chunk, doc_starts):
+        if reset:
+            W = w0.copy()
+        out[s:e] = z[s:e] @ W.T
+        W = W + float(eta) * (v[s:e].T @ z[s:e])
     return out, W
 
 

@@ -247,6 +247,34 @@ def test_brute_force_tiny(case):
     assert _rel(w, wb) < 1e-12
 
 
+def _torch_intermediates(cfg):
+    """Z from torch's Linear and SiLU, and V chunk by chunk from torch's
+    depthwise conv1d and a matmul, over the chunks the call makes."""
+    x = _t(cfg["x"])
+    z = (F.silu(F.linear(x, _t(cfg["w_gate"]))) * F.linear(x, _t(cfg["w_up"]))).numpy()
+    v = np.zeros((x.shape[0], cfg["d"]))
+    cuts = sorted(set(cfg["doc_starts"]) | {0, cfg["T"]})
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        for s in range(a, b, cfg["chunk"]):
+            e = min(s + cfg["chunk"], b)
+            v[s:e] = _torch_target_source(cfg["x0"][s:e], cfg["conv_w"]) @ np.float64(cfg["w_target"])
+    return z, v
+
+
+@pytest.mark.parametrize("case", BRUTE_CASES)
+def test_core_recursion_matches_brute_force(case):
+    """The apply+update recursion on library-computed Z and V equals the
+    scalar restatement of the whole method."""
+    cfg = _tiny(T=case["T"], C=case["C"], k=case["k"], doc_starts=case["doc_starts"])
+    z, v = _torch_intermediates(cfg)
+    o, w = orc.ttt_core(z, v, cfg["w_down0"], cfg["eta"], cfg["chunk"], cfg["doc_starts"])
+    ob, wb = brute_force_layer(cfg["x"], cfg["x0"], cfg["w_gate"], cfg["w_up"], cfg["w_down0"],
+                               cfg["conv_w"], cfg["w_target"], cfg["eta"], cfg["chunk"],
+                               cfg["doc_starts"])
+    assert _rel(o, ob) < 1e-12
+    assert _rel(w, wb) < 1e-12
+
+
 @pytest.mark.parametrize("mode,tau", [(1, None), (2, None), (0, 0.05), (2, 0.02), (1, 1e9)])
 def test_brute_force_target_modes_and_clipping(mode, tau):
     cfg = _tiny(T=13, C=4, k=3, doc_starts=(0, 9), eta=0.8)
@@ -489,6 +517,7 @@ def _pins_pass(module_overrides):
             lambda: test_brute_force_target_modes_and_clipping(0, 0.05),
             lambda: test_brute_force_target_modes_and_clipping(2, None),
             lambda: test_target_modes_match_torch_conv1d(2, 5, 9),
+            lambda: test_core_recursion_matches_brute_force(BRUTE_CASES[3]),
         ]
         for c in checks:
             try:
@@ -512,6 +541,31 @@ def _update_before_apply(x, x0, w_gate, w_up, w_down0, conv_w, w_target, eta, ch
         z = orc.swiglu_intermediate(x[s:e], w_gate, w_up)
         W = W + eta * (orc.chunk_target(x0[s:e], conv_w, w_target).T @ z)
         out[s:e] = z @ W.T
+    return out, W
+
+
+def _core_update_before_apply(z, v, w_down0, eta, chunk, doc_starts=(0,), w_init=None):
+    z, v, w0 = map(np.float64, (z, v, w_down0))
+    W = w0.copy()
+    out = np.zeros((z.shape[0], w0.shape[0]))
+    for s, e, reset in orc.chunk_spans(z.shape[0], chunk, doc_starts):
+        if reset:
+            W = w0.copy()
+        W = W + eta * (v[s:e].T @ z[s:e])
+        out[s:e] = z[s:e] @ W.T
+    return out, W
+
+
+def _core_misaligned_update(z, v, w_down0, eta, chunk, doc_starts=(0,), w_init=None):
+    # each token's Z paired with another token's target (rows reversed in the chunk)
+    z, v, w0 = map(np.float64, (z, v, w_down0))
+    W = w0.copy()
+    out = np.zeros((z.shape[0], w0.shape[0]))
+    for s, e, reset in orc.chunk_spans(z.shape[0], chunk, doc_starts):
+        if reset:
+            W = w0.copy()
+        out[s:e] = z[s:e] @ W.T
+        W = W + eta * (v[s:e][::-1].T @ z[s:e])
     return out, W
 
 
@@ -569,6 +623,8 @@ def test_planted_mistakes_are_caught():
         "clipping ignored": {"clip_delta": lambda delta, tau: delta},
         "clipping by max-abs, not Frobenius": {"clip_delta": _clip_by_max},
         "causal window shifted by one token": {"chunk_target_source": _causal_off_by_one},
+        "core: update before apply": {"ttt_core": _core_update_before_apply},
+        "core: a chunk's target rows paired with the wrong tokens": {"ttt_core": _core_misaligned_update},
     }
     for name, ov in mistakes.items():
         assert not _pins_pass(ov), f"planted mistake not caught: {name}"
