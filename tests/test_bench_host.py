@@ -44,3 +44,23 @@ def test_traffic_withheld_for_another_shape_or_kernel(tmp_path, monkeypatch):
     path.write_text(json.dumps(stale))
     monkeypatch.setattr(b, "TRAFFIC_FILE", str(path))
     assert b.stored_traffic(16, rec["captured_chunk"], shape["d"], shape["f"]) is None
+
+
+def test_peak_follows_the_sampled_clock():
+    b = _bench()
+    peaks = {"bf16_tflops": 1757.8, "bf16_tflops_sustained": 1370.5, "sm_max_mhz": 2032.0}
+    # a short region at the maximum clock: the burst figure
+    assert b.pick_peak(peaks, {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0}) == (1757.8, "bf16_tflops")
+    assert b.pick_peak(peaks, {"sm_mhz": 1900.0, "sm_max_mhz": 2032.0}) == (1757.8, "bf16_tflops")
+    # a long, power-capped region: the sustained figure
+    assert b.pick_peak(peaks, {"sm_mhz": 1215.0, "sm_max_mhz": 2032.0}) == (1370.5, "bf16_tflops_sustained")
+    # no clock record: the burst figure (the larger denominator)
+    assert b.pick_peak(peaks, {"sm_mhz": None, "sm_max_mhz": None})[1] == "bf16_tflops"
+
+
+def test_core_cpu_sample_runs_the_oracle_recursion():
+    b = _bench()
+    from ttt_inputs import make_layer
+    cfg = make_layer(16, 32, 40, 8, 3, 0.1, dtype="bf16", seed=0, init="qwen")
+    v, n, dt = b.oracle_core_sample(cfg, 0.0)
+    assert n >= 16 and n % 8 == 0 and v > 0 and dt > 0
