@@ -37,6 +37,11 @@ design notes):
       edges like R1: mode 1 starts at the current token (k = 1 is the
       reconstruction target X0[t]); mode 2 is a causal window that ends at the
       next token.
+  R13 Placement ([SUM] C.3 "TTT integration"; [BLOG] 6 and FAQ): with TTT in
+      every s-th MLP block, the TTT blocks are the s-th, 2s-th, ... blocks
+      counted from 1 (0-based l with (l + 1) % s == 0); every other block is
+      the unchanged SwiGLU MLP with its frozen W_down.  s = 1 puts TTT in
+      every block.
 
 Function-level parity status: every public function here is pinned by a
 "not gpu" test (brute force, closed forms, library routines, invariants).
@@ -60,6 +65,7 @@ __all__ = [
     "ttt_core",
     "ttt_layer_rows",
     "rms_norm",
+    "static_mlp",
     "ttt_stack",
 ]
 
@@ -271,23 +277,36 @@ def rms_norm(h, eps=1e-6) -> np.ndarray:
     return h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + eps)
 
 
-def ttt_stack(h0, layers, eta, chunk, doc_starts=(0,), eps=1e-6, n_layers=None,
-              x0=None, target_mode=TARGET_NEXT, clip_tau=None):
-    """Stack of pre-norm residual SwiGLU+TTT MLP blocks (no attention).
+def static_mlp(x, w_gate, w_up, w_down) -> np.ndarray:
+    """The ordinary SwiGLU MLP block, Z W_down^T with Z = SiLU(X W_gate^T) *
+    (X W_up^T): a block that does not carry TTT ([SUM] C.3; reading R13)."""
+    return swiglu_intermediate(x, w_gate, w_up) @ _f64(w_down).T
 
-    h_{l+1} = h_l + TTT_MLP_l(RMSNorm(h_l)) with X0 = h_0 for every layer
-    (X0 is the embedding sequence fed to the stack, [BLOG] 4).  ``x0`` is that
-    embedding sequence as stored for the layers (default: h0 itself).  Each
-    layer's recursion runs over all tokens before the next layer starts; that
-    is the same computation because nothing mixes tokens across layers except
-    the per-layer chunk recursion.  Returns (h_L, list of final W per layer)."""
+
+def ttt_stack(h0, layers, eta, chunk, doc_starts=(0,), eps=1e-6, n_layers=None,
+              x0=None, target_mode=TARGET_NEXT, clip_tau=None, ttt_every=1):
+    """Stack of pre-norm residual SwiGLU MLP blocks (no attention).
+
+    h_{l+1} = h_l + MLP_l(RMSNorm(h_l)) with X0 = h_0 for every TTT block (X0
+    is the embedding sequence fed to the stack, [BLOG] 4).  MLP_l is a
+    TTT-MLP block when (l + 1) % ttt_every == 0 and the static SwiGLU MLP
+    otherwise (reading R13; [SUM] C.3 puts TTT in every sixth block).
+    ``x0`` is that embedding sequence as stored for the layers (default: h0
+    itself).  Each layer's recursion runs over all tokens before the next
+    layer starts; that is the same computation because nothing mixes tokens
+    across layers except the per-layer chunk recursion.  Returns (h_L, list of
+    the final W per layer; a static block's is its W_down)."""
     h = _f64(h0).copy()
     x0 = _f64(h0 if x0 is None else x0)
     finals = []
     for li, w in enumerate(layers[: n_layers or len(layers)]):
-        o, wf = ttt_layer(rms_norm(h, eps), x0, w["w_gate"], w["w_up"], w["w_down0"],
-                          w["conv_w"], w["w_target"], eta, chunk, doc_starts,
-                          target_mode=target_mode, clip_tau=clip_tau)
+        xn = rms_norm(h, eps)
+        if (li + 1) % ttt_every == 0:
+            o, wf = ttt_layer(xn, x0, w["w_gate"], w["w_up"], w["w_down0"],
+                              w["conv_w"], w["w_target"], eta, chunk, doc_starts,
+                              target_mode=target_mode, clip_tau=clip_tau)
+        else:
+            o, wf = static_mlp(xn, w["w_gate"], w["w_up"], w["w_down0"]), _f64(w["w_down0"])
         h = h + o
         finals.append(wf)
     return h, finals

@@ -492,6 +492,39 @@ def test_stack_matches_brute_force_composition():
     assert _rel(h, hb) < 1e-12
 
 
+@pytest.mark.parametrize("every", [1, 2, 3])
+def test_stack_placement_matches_brute_force_composition(every):
+    """TTT in every `every`-th block (1-based), the others the plain SwiGLU
+    MLP: brute force for the TTT blocks and torch's Linear/SiLU MLP for the
+    static ones, composed with torch's rms_norm."""
+    from ttt_inputs import make_stack
+    h0, layers, meta = make_stack(4, 4, 8, 10, 4, 2, 0.5, seed=5, dtype="f32")
+    h, finals = orc.ttt_stack(h0, layers, meta["eta"], meta["chunk"], ttt_every=every)
+    hb = np.float64(h0)
+    for li, w in enumerate(layers):
+        xn = F.rms_norm(_t(hb), (hb.shape[1],), eps=1e-6).numpy()
+        if (li + 1) % every == 0:
+            ob, wb = brute_force_layer(xn, h0, w["w_gate"], w["w_up"], w["w_down0"], w["conv_w"],
+                                       w["w_target"], meta["eta"], meta["chunk"])
+        else:
+            ob, wb = _torch_static_mlp(xn, w["w_gate"], w["w_up"], w["w_down0"]), w["w_down0"]
+        hb = hb + ob
+        assert _rel(finals[li], wb) < 1e-12
+    assert _rel(h, hb) < 1e-12
+    if every == 1:
+        h1, _ = orc.ttt_stack(h0, layers, meta["eta"], meta["chunk"])
+        assert np.array_equal(h, h1)
+
+
+def test_static_mlp_matches_torch_and_eta_zero_layer():
+    cfg = _tiny(d=8, f=24, T=11, C=4, k=3)
+    ref = _torch_static_mlp(cfg["x"], cfg["w_gate"], cfg["w_up"], cfg["w_down0"])
+    o = orc.static_mlp(cfg["x"], cfg["w_gate"], cfg["w_up"], cfg["w_down0"])
+    assert _rel(o, ref) < 1e-14
+    o0, _ = _run(cfg, eta=0.0)
+    assert _rel(o, o0) < 1e-14
+
+
 def test_bf16_inputs_are_exact_in_oracle():
     """The oracle sees exactly the stored (bf16-rounded) input values."""
     cfg = make_layer(16, 32, 8, 4, 2, 1e-3, dtype="bf16", init="qwen")
@@ -518,6 +551,7 @@ def _pins_pass(module_overrides):
             lambda: test_brute_force_target_modes_and_clipping(2, None),
             lambda: test_target_modes_match_torch_conv1d(2, 5, 9),
             lambda: test_core_recursion_matches_brute_force(BRUTE_CASES[3]),
+            lambda: test_stack_placement_matches_brute_force_composition(3),
         ]
         for c in checks:
             try:
@@ -609,6 +643,23 @@ def _clip_by_max(delta, tau):
     return delta * (tau / m) if tau and m > tau else delta
 
 
+def _stack_placement_from_zero(h0, layers, eta, chunk, doc_starts=(0,), eps=1e-6, n_layers=None,
+                               x0=None, target_mode=0, clip_tau=None, ttt_every=1):
+    # TTT in blocks 0, s, 2s, ... instead of the s-th, 2s-th, ... (1-based)
+    h = np.float64(h0).copy()
+    finals = []
+    for li, w in enumerate(layers[: n_layers or len(layers)]):
+        xn = orc.rms_norm(h, eps)
+        if li % ttt_every == 0:
+            o, wf = orc.ttt_layer(xn, np.float64(h0), w["w_gate"], w["w_up"], w["w_down0"],
+                                  w["conv_w"], w["w_target"], eta, chunk, doc_starts)
+        else:
+            o, wf = orc.static_mlp(xn, w["w_gate"], w["w_up"], w["w_down0"]), np.float64(w["w_down0"])
+        h = h + o
+        finals.append(wf)
+    return h, finals
+
+
 def test_planted_mistakes_are_caught():
     assert _pins_pass({})
     mistakes = {
@@ -624,6 +675,7 @@ def test_planted_mistakes_are_caught():
         "clipping by max-abs, not Frobenius": {"clip_delta": _clip_by_max},
         "causal window shifted by one token": {"chunk_target_source": _causal_off_by_one},
         "core: update before apply": {"ttt_core": _core_update_before_apply},
+        "placement counted from block 0": {"ttt_stack": _stack_placement_from_zero},
         "core: a chunk's target rows paired with the wrong tokens": {"ttt_core": _core_misaligned_update},
     }
     for name, ov in mistakes.items():
