@@ -571,12 +571,30 @@ def run_extra(args):
     else:
         c = CONFIGS["stack"]
         h0, layers = make_stack_device(c["n_layers"], c["d"], c["f"], c["T"], c["k"], seed=0)
-        stack = TTTStack(layers, chunk=c["chunk"], eta=c["eta"], max_tokens=c["T"])
-        sec, clk = timed(lambda: stack(h0), max(3, min(steps, 5)), 1)
-        emit(f"{c['n_layers']}-layer stack (tokens through all layers)", c["T"], sec, clk,
-             {"workload": "stack", "n_layers": c["n_layers"], "d": c["d"], "f": c["f"],
-              "T": c["T"], "chunk": c["chunk"],
-              "layer_tokens_per_s": c["n_layers"] * c["T"] / sec})
+        for every in (1, 6):
+            stack = TTTStack(layers, chunk=c["chunk"], eta=c["eta"], max_tokens=c["T"],
+                             ttt_every=every)
+            sec, clk = timed(lambda: stack(h0), max(3, min(steps, 5)), 1)
+            stack.check()
+            n_ttt = sum(1 for li in range(c["n_layers"]) if (li + 1) % every == 0)
+            emit(f"{c['n_layers']}-layer stack, TTT in every {every} block(s) "
+                 f"(tokens through all layers)", c["T"], sec, clk,
+                 {"workload": "stack", "n_layers": c["n_layers"], "ttt_every": every,
+                  "ttt_layers": n_ttt, "d": c["d"], "f": c["f"], "T": c["T"], "chunk": c["chunk"],
+                  "layer_tokens_per_s": c["n_layers"] * c["T"] / sec})
+            stack.close()
+            del stack
+        # the single TTT layer on the same shape, for the per-layer comparison
+        w = layers[0]
+        single = TTTMLP(w["w_gate"], w["w_up"], w["w_down0"], w["conv_w"], w["w_target"],
+                        chunk=c["chunk"], eta=c["eta"], max_tokens=c["T"])
+        x = h0.to(torch.bfloat16)
+        o = torch.empty_like(x)
+        sec, clk = timed(lambda: single.forward(x, doc_starts=(0,), out=o), steps, args.warmup)
+        single.check()
+        emit("single TTT layer of the stack's shape", c["T"], sec, clk,
+             {"workload": "stack-single-layer", "d": c["d"], "f": c["f"], "T": c["T"],
+              "chunk": c["chunk"]})
     return 0
 
 

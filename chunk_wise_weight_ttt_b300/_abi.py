@@ -35,7 +35,12 @@ SIGNATURES = {
     "ttt_mlp_workspace_bytes": (C.c_size_t, [C.POINTER(Config)]),
     "ttt_mlp_create": (_st, [C.POINTER(Config), _vp, _vp, _vp, _vp, _vp, _vp, C.c_size_t, _vp,
                              C.POINTER(_vp)]),
+    "ttt_mlp_state_bytes": (C.c_size_t, [C.POINTER(Config)]),
+    "ttt_mlp_scratch_bytes": (C.c_size_t, [C.POINTER(Config)]),
+    "ttt_mlp_create_split": (_st, [C.POINTER(Config), _vp, _vp, _vp, _vp, _vp, _vp, C.c_size_t, _vp,
+                                   C.c_size_t, _vp, C.POINTER(_vp)]),
     "ttt_mlp_forward_chunks": (_st, [_vp, _i32, _vp, _vp, _i64, C.POINTER(_i64), _i32, _vp, _vp]),
+    "ttt_mlp_forward_static": (_st, [_vp, _vp, _i64, _vp, _vp]),
     "ttt_mlp_forward_chunks_host": (_st, [_vp, _i32, _vp, _vp, _i64, C.POINTER(_i64), _i32, _vp,
                                           _vp]),
     "ttt_mlp_reset": (_st, [_vp, _i32, _vp]),

@@ -28,7 +28,10 @@
 //   kSwiGLU  Z = SiLU(X Wg^T) (.) (X Wu^T): the B tile stacks 128 rows of Wg
 //            and the same 128 rows of Wu, so one 128x256 accumulator holds the
 //            gate and up halves of a 128x128 block of Z.
-//   kVProj   V = eta * (U W_target) with U the chunk-local Conv1D output.
+//   kLinear  out = alpha * (A B^T) over a K range of `kdim`: the target
+//            projection V = eta * (U W_target) (A = U, the chunk-local Conv1D
+//            output, B = W_target^T, K = d) and the static MLP's down
+//            projection O = Z W_0^T (A = Z, B = W_0, K = f).
 //   kSGram   per group of chunks, S = Z_g Z_g^T with every entry whose column
 //            chunk is not strictly before its row chunk set to zero.
 //   kDGram   per group of chunks, the same-chunk (block-diagonal) entries of
@@ -88,11 +91,11 @@ constexpr int kWBoxes = kBN / kWBoxCols;
 constexpr int kStgBytesPerWarp = 32 * 128;
 constexpr int kEpiWarps = 4;
 
-enum GemmMode : int { kSwiGLU = 0, kVProj = 1, kSGram = 2, kGroup = 3, kDGram = 4 };
+enum GemmMode : int { kSwiGLU = 0, kLinear = 1, kSGram = 2, kGroup = 3, kDGram = 4 };
 
 // Tensor-map slots per mode (B boxes are the half that one CTA of a pair holds).
 //   kSwiGLU: 0 X (box 64x128), 1 Wg (64x128), 2 Wu (64x128)
-//   kVProj:  0 U (64x128), 1 W_target^T (64x128)
+//   kLinear: 0 A (64x128), 1 B (64x128)
 //   kSGram:  0 Z (64x128), 1 Z (64x128)
 //   kDGram:  0 Z or V (64x128), 1 the same (64x128); `f` holds its width
 //   kGroup:  0 Z (64x128), 1 Wb[0] (64x128), 2 S (64x128),
@@ -112,10 +115,11 @@ struct GemmArgs {
   int n_rows;    // tokens of the call (rows of X/Z/U/V/O)
   int d, f;
   int chunk;
-  float alpha;   // eta for kVProj
+  float alpha;   // kLinear: the output scale (eta for the target projection)
+  int kdim;      // kLinear: the K extent (d for the target projection, f for O = Z W_0^T)
   int* counter;  // dynamic tile-pair counter, zero at launch
   int* err;      // workspace error word
-  void* out0;    // kSwiGLU: Z; kVProj: V; kSGram: S; kGroup: O
+  void* out0;    // kSwiGLU: Z; kLinear: V or O (n_rows x d); kSGram: S; kGroup: O
   void* out1;    // kGroup: W (fp32, updated in place)
   void* wb[2];   // kGroup: the two bf16 copies of the state (read / written alternately)
   const void* w0;  // kGroup: W_0 (bf16)
@@ -161,7 +165,7 @@ __device__ __forceinline__ int corr_kbound(int len, int m, int chunk) {
 template <int MODE>
 __device__ __forceinline__ int num_tiles(const GemmArgs& a) {
   if (MODE == kSwiGLU) return cdiv(cdiv(a.n_rows, kBM), 2) * cdiv(a.f, kBM);
-  if (MODE == kVProj) return cdiv(cdiv(a.n_rows, kBM), 2) * cdiv(a.d, kBN);
+  if (MODE == kLinear) return cdiv(cdiv(a.n_rows, kBM), 2) * cdiv(a.d, kBN);
   if (MODE == kSGram || MODE == kDGram)
     return a.n_groups * cdiv(cdiv(a.s_pad, kBM), 2) * cdiv(a.s_pad, kBN);
   return a.g_tile[a.n_groups];
@@ -199,11 +203,11 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int ra
     ti.m0 = (2 * (first + w % gm) + rank) * kBM;
     ti.n0 = (w / gm) * kBM;
     ti.nkb1 = cdiv(a.d, kBK);
-  } else if (MODE == kVProj) {
+  } else if (MODE == kLinear) {
     const int nt = cdiv(a.d, kBN);
     ti.m0 = (2 * (t / nt) + rank) * kBM;
     ti.n0 = (t % nt) * kBN;
-    ti.nkb1 = cdiv(a.d, kBK);
+    ti.nkb1 = cdiv(a.kdim, kBK);
   } else if (MODE == kSGram) {
     const int mpt = cdiv(cdiv(a.s_pad, kBM), 2), nt = cdiv(a.s_pad, kBN);
     const int g = t / (mpt * nt), r = t % (mpt * nt);
@@ -275,7 +279,7 @@ __device__ __forceinline__ void load_kblock(const GemmArgs& a, const TileInfo& t
   if (MODE == kSwiGLU) {
     tma_load_2d_pair(sa, &a.map[0], bar, kb * kBK, ti.m0);
     tma_load_2d_pair(sb, &a.map[1 + rank], bar, kb * kBK, ti.n0);
-  } else if (MODE == kVProj) {
+  } else if (MODE == kLinear) {
     tma_load_2d_pair(sa, &a.map[0], bar, kb * kBK, ti.m0);
     tma_load_2d_pair(sb, &a.map[1], bar, kb * kBK, ti.n0 + rank * kh);
   } else if (MODE == kSGram || MODE == kDGram) {
@@ -380,7 +384,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
       const int col = ti.n0 + s * 32;
       if (grow < a.n_rows) store_bf16x32(zrow + col, p, a.f - col);
     }
-  } else if (MODE == kVProj || MODE == kGroup) {
+  } else if (MODE == kLinear || MODE == kGroup) {
     if (MODE == kGroup && ti.kind == 1) {
       // fast-weight update: W <- W_s + acc (acc = V^T Z of the group, from
       // zero), one fp32 rounding.  Each 32-column slice of the warp's 32 rows
@@ -449,10 +453,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
         for (int j = 0; j < 8; ++j) wc[j] = wn[j];
       }
     } else {
-      // plain bf16 store of alpha * acc (kVProj) or acc (kGroup apply)
-      const float alpha = (MODE == kVProj) ? a.alpha : 1.0f;
-      const int grow = (MODE == kVProj) ? ti.m0 + row : a.g_start[ti.g] + ti.m0 + row;
-      const bool ok = (MODE == kVProj) ? (grow < a.n_rows) : (ti.m0 + row < a.g_len[ti.g]);
+      // plain bf16 store of alpha * acc (kLinear) or acc (kGroup apply)
+      const float alpha = (MODE == kLinear) ? a.alpha : 1.0f;
+      const int grow = (MODE == kLinear) ? ti.m0 + row : a.g_start[ti.g] + ti.m0 + row;
+      const bool ok = (MODE == kLinear) ? (grow < a.n_rows) : (ti.m0 + row < a.g_len[ti.g]);
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out0) + (size_t)grow * a.d;
 #pragma unroll 1
       for (int s = 0; s < kBN / 32; ++s) {

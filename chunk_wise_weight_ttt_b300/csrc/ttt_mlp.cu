@@ -25,8 +25,6 @@ using namespace ttt;
 struct ttt_mlp {
   ttt_mlp_config cfg;
   const void *wg, *wu, *w0, *conv, *wt;
-  uint8_t* ws;
-  size_t ws_bytes;
   bool tc;
   int G, L, s_pad, s_slots, num_sms;
   int max_pairs;            // co-resident CTA pairs of the tcgen05 kernels
@@ -97,10 +95,16 @@ int group_tokens() {
   return g;
 }
 
+// Workspace layout.  The state part (control block, fast weights, their bf16
+// operand copies, the transposed W_target) belongs to one handle; the scratch
+// part (per-call intermediates and host staging) may be shared by handles
+// whose calls are ordered one after another.  Offsets of each part are
+// relative to that part's base.
 struct Layout {
   bool tc;
   int G, L, s_pad, s_slots;
-  size_t ctrl, W, Wb0, Wb1, WtT, Z, U, V, S, GZ, GV, xs, x0s, os, total;
+  size_t ctrl, W, Wb0, Wb1, WtT, state_total;              // state part
+  size_t Z, U, V, S, GZ, GV, xs, x0s, os, scratch_total;    // scratch part
 };
 
 bool config_ok(const ttt_mlp_config* c, std::string* why) {
@@ -148,6 +152,8 @@ Layout make_layout(const ttt_mlp_config& c, bool tc) {
   l.Wb0 = tc ? take(d * f * 2) : 0;
   l.Wb1 = tc ? take(d * f * 2) : 0;
   l.WtT = tc ? take(d * d * 2) : 0;
+  l.state_total = o;
+  o = 0;
   l.Z = take(n * f * inter);
   l.U = take(n * d * inter);
   l.V = take(n * d * inter);
@@ -162,8 +168,21 @@ Layout make_layout(const ttt_mlp_config& c, bool tc) {
   l.xs = take(n * d * act);
   l.x0s = take(n * d * act);
   l.os = take(n * d * act);
-  l.total = o;
+  l.scratch_total = o;
   return l;
+}
+
+// Bytes of each part the handle may need: the larger of the two kernel
+// families' layouts (which family runs is decided at create).
+size_t state_bytes_of(const ttt_mlp_config& c) {
+  size_t b = make_layout(c, false).state_total;
+  if (tc_shape_ok(c)) b = std::max(b, make_layout(c, true).state_total);
+  return b;
+}
+size_t scratch_bytes_of(const ttt_mlp_config& c) {
+  size_t b = make_layout(c, false).scratch_total;
+  if (tc_shape_ok(c)) b = std::max(b, make_layout(c, true).scratch_total);
+  return b;
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -314,10 +333,10 @@ cudaError_t launch_gemm(ttt_mlp* h, GemmArgs& a, int npairs, cudaStream_t st) {
 // Kernel attributes of the tcgen05 engine and the number of CTA pairs that can
 // be resident at once (0 on failure).
 cudaError_t setup_tc_kernels(int* max_pairs) {
-  const void* kfn[5] = {(const void*)tc_gemm_kernel<kSwiGLU>, (const void*)tc_gemm_kernel<kVProj>,
+  const void* kfn[5] = {(const void*)tc_gemm_kernel<kSwiGLU>, (const void*)tc_gemm_kernel<kLinear>,
                         (const void*)tc_gemm_kernel<kSGram>, (const void*)tc_gemm_kernel<kGroup>,
                         (const void*)tc_gemm_kernel<kDGram>};
-  const int smem[5] = {smem_bytes_of<kSwiGLU>(), smem_bytes_of<kVProj>(), smem_bytes_of<kSGram>(),
+  const int smem[5] = {smem_bytes_of<kSwiGLU>(), smem_bytes_of<kLinear>(), smem_bytes_of<kSGram>(),
                        smem_bytes_of<kGroup>(), smem_bytes_of<kDGram>()};
   for (int i = 0; i < 5; ++i) {
     cudaError_t e = cudaFuncSetAttribute(kfn[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
@@ -452,10 +471,11 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
   a.map[1] = h->map_wtT;
   a.out0 = h->V;
   a.alpha = c.eta;
+  a.kdim = d;
   a.counter = next_counter(h, st);
   a.test_withhold_block = fault_injected("kernel_wait") ? 1 : 0;
   pt.begin(2);
-  TTT_CK(h, launch_gemm<kVProj>(h, a, cdiv_h(cdiv_h((int)n, kBM), 2) * cdiv_h(d, kBN), st));
+  TTT_CK(h, launch_gemm<kLinear>(h, a, cdiv_h(cdiv_h((int)n, kBM), 2) * cdiv_h(d, kBN), st));
   a.test_withhold_block = 0;
   pt.end();
   h->prof_launches++;
@@ -597,6 +617,57 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
     }
     pt.end();
   }
+  return TTT_OK;
+}
+
+// The block's static MLP, O = SwiGLU(X) W_0^T, on the tcgen05 path: the
+// SwiGLU producer, then O = Z W_0^T with the plain GEMM tiles.  No fast
+// weight is read or written.
+ttt_status forward_static_tc(ttt_mlp* h, const void* x, int64_t n, void* o, cudaStream_t st) {
+  const ttt_mlp_config& c = h->cfg;
+  const int d = c.d, f = c.f;
+  std::string why;
+  CUtensorMap map_x, map_z;
+  if (!make_map(&map_x, x, d, n, d, 64, 128, &why) || !make_map(&map_z, h->Z, f, n, f, 64, 128, &why))
+    return fail(h, TTT_ECUDA, why);
+  TTT_CK(h, cudaMemsetAsync(h->ctrl + kCounterBase, 0, (kCtrlInts - kCounterBase) * sizeof(int), st));
+  h->counter_next = kCounterBase;
+  GemmArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.n_rows = (int)n;
+  a.d = d;
+  a.f = f;
+  a.chunk = c.chunk;
+  a.err = h->ctrl;
+  a.map[0] = map_x;
+  a.map[1] = h->map_wg;
+  a.map[2] = h->map_wu;
+  a.out0 = h->Z;
+  a.counter = next_counter(h, st);
+  TTT_CK(h, launch_gemm<kSwiGLU>(h, a, cdiv_h(cdiv_h((int)n, kBM), 2) * cdiv_h(f, kBM), st));
+  a.map[0] = map_z;
+  a.map[1] = h->map_w0;
+  a.kdim = f;
+  a.alpha = 1.0f;
+  a.out0 = o;
+  a.counter = next_counter(h, st);
+  TTT_CK(h, launch_gemm<kLinear>(h, a, cdiv_h(cdiv_h((int)n, kBM), 2) * cdiv_h(d, kBN), st));
+  h->prof_launches += 2;
+  return TTT_OK;
+}
+
+template <typename T>
+ttt_status forward_static_simt(ttt_mlp* h, const void* xv, int64_t n, void* ov, cudaStream_t st) {
+  const int d = h->cfg.d, f = h->cfg.f, nn = (int)n;
+  float* Z = (float*)h->Z;
+  dim3 gz((f + 63) / 64, (nn + 63) / 64);
+  simt_swiglu_kernel<T><<<gz, 256, 0, st>>>(nn, f, d, (const T*)xv, (const T*)h->wg, (const T*)h->wu, Z);
+  TTT_CK_LAUNCH(h);
+  dim3 ga((d + 63) / 64, (nn + 63) / 64);
+  simt_gemm_kernel<float, T, T><<<ga, 256, 0, st>>>(nn, d, f, Z, f, 1, (const T*)h->w0, 1, f, (T*)ov, d,
+                                                    1.0f, 0.0f);
+  TTT_CK_LAUNCH(h);
+  h->prof_launches += 2;
   return TTT_OK;
 }
 
@@ -771,14 +842,25 @@ extern "C" {
 size_t ttt_mlp_workspace_bytes(const ttt_mlp_config* cfg) {
   std::string why;
   if (!config_ok(cfg, &why)) return 0;
-  size_t b = make_layout(*cfg, false).total;
-  if (tc_shape_ok(*cfg)) b = std::max(b, make_layout(*cfg, true).total);
-  return b;
+  return align_up(state_bytes_of(*cfg), 256) + scratch_bytes_of(*cfg);
 }
 
-ttt_status ttt_mlp_create(const ttt_mlp_config* cfg, const void* w_gate, const void* w_up,
-                          const void* w_down0, const void* conv_w, const void* w_target,
-                          void* workspace, size_t workspace_bytes, void* stream, ttt_mlp** out) {
+size_t ttt_mlp_state_bytes(const ttt_mlp_config* cfg) {
+  std::string why;
+  if (!config_ok(cfg, &why)) return 0;
+  return state_bytes_of(*cfg);
+}
+
+size_t ttt_mlp_scratch_bytes(const ttt_mlp_config* cfg) {
+  std::string why;
+  if (!config_ok(cfg, &why)) return 0;
+  return scratch_bytes_of(*cfg);
+}
+
+ttt_status ttt_mlp_create_split(const ttt_mlp_config* cfg, const void* w_gate, const void* w_up,
+                                const void* w_down0, const void* conv_w, const void* w_target,
+                                void* state, size_t state_bytes, void* scratch, size_t scratch_bytes,
+                                void* stream, ttt_mlp** out) {
   if (fault_injected("create")) return fail(nullptr, TTT_EFAULT_INJECTED, "fault injected: create");
   if (!out) return fail(nullptr, TTT_EINVAL, "out is NULL");
   *out = nullptr;
@@ -789,11 +871,18 @@ ttt_status ttt_mlp_create(const ttt_mlp_config* cfg, const void* w_gate, const v
     if (!p) return fail(nullptr, TTT_EINVAL, "weight pointers must be non-NULL");
     if (!aligned16(p)) return fail(nullptr, TTT_EINVAL, "weight pointers must be 16-byte aligned");
   }
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return fail(nullptr, TTT_EINVAL, "workspace must be non-NULL and 256-byte aligned");
+  if (!state || (reinterpret_cast<uintptr_t>(state) & 255u) || !scratch ||
+      (reinterpret_cast<uintptr_t>(scratch) & 255u))
+    return fail(nullptr, TTT_EINVAL, "state and scratch must be non-NULL and 256-byte aligned");
   const bool tc = tc_shape_ok(*cfg) && !force_simt();
   const Layout l = make_layout(*cfg, tc);
-  if (workspace_bytes < l.total) return fail(nullptr, TTT_EINVAL, "workspace is smaller than ttt_mlp_workspace_bytes()");
+  if (state_bytes < l.state_total || scratch_bytes < l.scratch_total)
+    return fail(nullptr, TTT_EINVAL, "state or scratch is smaller than ttt_mlp_state_bytes() / ttt_mlp_scratch_bytes()");
+  {
+    const uintptr_t a0 = (uintptr_t)state, b0 = (uintptr_t)scratch;
+    if (a0 < b0 + l.scratch_total && b0 < a0 + l.state_total)
+      return fail(nullptr, TTT_EINVAL, "state and scratch must not overlap");
+  }
 
   ttt_mlp* h = new ttt_mlp();
   h->cfg = *cfg;
@@ -802,27 +891,27 @@ ttt_status ttt_mlp_create(const ttt_mlp_config* cfg, const void* w_gate, const v
   h->w0 = w_down0;
   h->conv = conv_w;
   h->wt = w_target;
-  h->ws = (uint8_t*)workspace;
-  h->ws_bytes = workspace_bytes;
   h->tc = tc;
   h->G = l.G;
   h->L = l.L;
   h->s_pad = l.s_pad;
   h->s_slots = l.s_slots;
-  h->ctrl = (int*)(h->ws + l.ctrl);
-  h->W = (float*)(h->ws + l.W);
-  h->Wb[0] = (__nv_bfloat16*)(h->ws + l.Wb0);
-  h->Wb[1] = (__nv_bfloat16*)(h->ws + l.Wb1);
-  h->WtT = (__nv_bfloat16*)(h->ws + l.WtT);
-  h->Z = h->ws + l.Z;
-  h->U = h->ws + l.U;
-  h->V = h->ws + l.V;
-  h->S = (__nv_bfloat16*)(h->ws + l.S);
-  h->GZ = l.GZ ? (float*)(h->ws + l.GZ) : nullptr;
-  h->GV = l.GV ? (float*)(h->ws + l.GV) : nullptr;
-  h->xs = h->ws + l.xs;
-  h->x0s = h->ws + l.x0s;
-  h->os = h->ws + l.os;
+  uint8_t* sb = (uint8_t*)state;
+  uint8_t* xb = (uint8_t*)scratch;
+  h->ctrl = (int*)(sb + l.ctrl);
+  h->W = (float*)(sb + l.W);
+  h->Wb[0] = (__nv_bfloat16*)(sb + l.Wb0);
+  h->Wb[1] = (__nv_bfloat16*)(sb + l.Wb1);
+  h->WtT = (__nv_bfloat16*)(sb + l.WtT);
+  h->Z = xb + l.Z;
+  h->U = xb + l.U;
+  h->V = xb + l.V;
+  h->S = (__nv_bfloat16*)(xb + l.S);
+  h->GZ = l.GZ ? (float*)(xb + l.GZ) : nullptr;
+  h->GV = l.GV ? (float*)(xb + l.GV) : nullptr;
+  h->xs = xb + l.xs;
+  h->x0s = xb + l.x0s;
+  h->os = xb + l.os;
   h->counter_next = kCounterBase;
   h->wb_owner = -1;
   h->wb_cur = 0;
@@ -872,6 +961,23 @@ ttt_status ttt_mlp_create(const ttt_mlp_config* cfg, const void* w_gate, const v
   return TTT_OK;
 }
 
+ttt_status ttt_mlp_create(const ttt_mlp_config* cfg, const void* w_gate, const void* w_up,
+                          const void* w_down0, const void* conv_w, const void* w_target,
+                          void* workspace, size_t workspace_bytes, void* stream, ttt_mlp** out) {
+  if (fault_injected("create")) return fail(nullptr, TTT_EFAULT_INJECTED, "fault injected: create");
+  if (!out) return fail(nullptr, TTT_EINVAL, "out is NULL");
+  *out = nullptr;
+  std::string why;
+  if (!config_ok(cfg, &why)) return fail(nullptr, TTT_EINVAL, why);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(nullptr, TTT_EINVAL, "workspace must be non-NULL and 256-byte aligned");
+  // the workspace is the state part followed by the scratch part
+  const size_t sb = align_up(state_bytes_of(*cfg), 256), xb = scratch_bytes_of(*cfg);
+  if (workspace_bytes < sb + xb) return fail(nullptr, TTT_EINVAL, "workspace is smaller than ttt_mlp_workspace_bytes()");
+  return ttt_mlp_create_split(cfg, w_gate, w_up, w_down0, conv_w, w_target, workspace, sb,
+                              (uint8_t*)workspace + sb, workspace_bytes - sb, stream, out);
+}
+
 ttt_status ttt_mlp_forward_chunks(ttt_mlp* h, int32_t doc, const void* x, const void* x0,
                                   int64_t n_tokens, const int64_t* doc_starts,
                                   int32_t n_doc_starts, void* o, void* stream) {
@@ -880,6 +986,17 @@ ttt_status ttt_mlp_forward_chunks(ttt_mlp* h, int32_t doc, const void* x, const 
   ttt_status s = validate_call(h, doc, x, x0, n_tokens, doc_starts, n_doc_starts, o);
   if (s != TTT_OK) return s;
   return forward_impl(h, doc, x, x0, n_tokens, doc_starts, n_doc_starts, o, (cudaStream_t)stream);
+}
+
+ttt_status ttt_mlp_forward_static(ttt_mlp* h, const void* x, int64_t n_tokens, void* o, void* stream) {
+  if (check_handle(h)) return TTT_EINVAL;
+  if (fault_injected("forward")) return fail(h, TTT_EFAULT_INJECTED, "fault injected: forward");
+  ttt_status s = validate_call(h, 0, x, x, n_tokens, nullptr, 0, o);
+  if (s != TTT_OK || n_tokens == 0) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (h->tc) return forward_static_tc(h, x, n_tokens, o, st);
+  if (h->cfg.act_dtype == TTT_BF16) return forward_static_simt<__nv_bfloat16>(h, x, n_tokens, o, st);
+  return forward_static_simt<float>(h, x, n_tokens, o, st);
 }
 
 ttt_status ttt_mlp_forward_chunks_host(ttt_mlp* h, int32_t doc, const void* x_host,
@@ -1179,12 +1296,13 @@ extern "C" ttt_status ttt_target_noalloc(const void* x0, const void* conv_w, con
   a.n_rows = (int)n_tokens;
   a.d = d;
   a.f = d;
+  a.kdim = d;
   a.chunk = chunk;
   a.alpha = eta;
   a.counter = ctrl;
   a.err = err;
   a.out0 = v;
   const int npairs = cdiv_h(cdiv_h((int)n_tokens, kBM), 2) * cdiv_h(d, kBN);
-  TTT_CK(nullptr, launch_pairs<kVProj>(pairs, a, npairs, st));
+  TTT_CK(nullptr, launch_pairs<kLinear>(pairs, a, npairs, st));
   return TTT_OK;
 }

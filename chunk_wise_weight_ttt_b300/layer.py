@@ -49,7 +49,7 @@ class TTTMLP:
     """
 
     def __init__(self, w_gate, w_up, w_down0, conv_w, w_target, *, chunk: int, eta: float,
-                 n_docs: int = 1, max_tokens: int, stream=None, workspace=None,
+                 n_docs: int = 1, max_tokens: int, stream=None, workspace=None, scratch=None,
                  target_mode: int = _abi.TTT_TARGET_NEXT, clip_tau: float = 0.0):
         self.lib = _abi.load()
         dt = w_gate.dtype
@@ -64,18 +64,33 @@ class TTTMLP:
         self.cfg = Config(d=d, f=f, chunk=chunk, conv_k=self.k, n_docs=n_docs, eta=eta,
                           act_dtype=_DT[dt], max_tokens=max_tokens, target_mode=target_mode,
                           clip_tau=clip_tau or 0.0)
-        nbytes = self.lib.ttt_mlp_workspace_bytes(C.byref(self.cfg))
-        if nbytes == 0:
-            raise TTTError(_abi.TTT_EINVAL, "invalid configuration")
-        if workspace is None:
-            workspace = torch.empty(nbytes, dtype=torch.uint8, device=w_gate.device)
-        elif workspace.dtype != torch.uint8 or workspace.numel() < nbytes or not workspace.is_cuda:
-            raise ValueError(f"workspace must be a CUDA uint8 tensor of at least {nbytes} bytes")
-        self.workspace = workspace
+        cfg = C.byref(self.cfg)
         self._weights = ws
         h = C.c_void_p()
-        st = self.lib.ttt_mlp_create(C.byref(self.cfg), *[_ptr(t) for t in ws], _ptr(self.workspace),
-                                     nbytes, _stream(stream), C.byref(h))
+        if scratch is None:
+            nbytes = self.lib.ttt_mlp_workspace_bytes(cfg)
+            if nbytes == 0:
+                raise TTTError(_abi.TTT_EINVAL, "invalid configuration")
+            if workspace is None:
+                workspace = torch.empty(nbytes, dtype=torch.uint8, device=w_gate.device)
+            elif workspace.dtype != torch.uint8 or workspace.numel() < nbytes or not workspace.is_cuda:
+                raise ValueError(f"workspace must be a CUDA uint8 tensor of at least {nbytes} bytes")
+            self.workspace = workspace
+            st = self.lib.ttt_mlp_create(cfg, *[_ptr(t) for t in ws], _ptr(self.workspace), nbytes,
+                                         _stream(stream), C.byref(h))
+        else:
+            # own state, scratch shared with other handles whose calls are ordered
+            sbytes = self.lib.ttt_mlp_state_bytes(cfg)
+            xbytes = self.lib.ttt_mlp_scratch_bytes(cfg)
+            if sbytes == 0:
+                raise TTTError(_abi.TTT_EINVAL, "invalid configuration")
+            if scratch.dtype != torch.uint8 or scratch.numel() < xbytes or not scratch.is_cuda:
+                raise ValueError(f"scratch must be a CUDA uint8 tensor of at least {xbytes} bytes")
+            self.state = torch.empty(sbytes, dtype=torch.uint8, device=w_gate.device)
+            self.workspace = scratch
+            st = self.lib.ttt_mlp_create_split(cfg, *[_ptr(t) for t in ws], _ptr(self.state), sbytes,
+                                               _ptr(scratch), scratch.numel(), _stream(stream),
+                                               C.byref(h))
         _check(self.lib, None, st)
         self.h = h
 
@@ -98,6 +113,15 @@ class TTTMLP:
         return out
 
     __call__ = forward
+
+    def forward_static(self, x: torch.Tensor, *, out: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+        """The block's static MLP, SwiGLU(x) W_0^T (no fast weight)."""
+        if out is None:
+            out = torch.empty_like(x)
+        st = self.lib.ttt_mlp_forward_static(self.h, _ptr(x), x.shape[0], _ptr(out), _stream(stream))
+        _check(self.lib, self.h, st)
+        return out
 
     def forward_host(self, x_host: torch.Tensor, x0_host: Optional[torch.Tensor] = None, *,
                      doc: int = 0, doc_starts: Optional[Sequence[int]] = (0,),
@@ -171,23 +195,36 @@ class TTTMLP:
 
 def workspace_bytes(d: int, f: int, *, chunk: int, conv_k: int, dtype=torch.bfloat16,
                     n_docs: int = 1, max_tokens: int, eta: float = 0.0,
-                    target_mode: int = _abi.TTT_TARGET_NEXT, clip_tau: float = 0.0) -> int:
-    """Device workspace (bytes) a layer of this shape needs."""
+                    target_mode: int = _abi.TTT_TARGET_NEXT, clip_tau: float = 0.0,
+                    part: str = "all") -> int:
+    """Device workspace (bytes) a layer of this shape needs: the whole
+    workspace (part="all"), or its per-handle state or shareable scratch part."""
     lib = _abi.load()
     cfg = Config(d=d, f=f, chunk=chunk, conv_k=conv_k, n_docs=n_docs, eta=eta, act_dtype=_DT[dtype],
                  max_tokens=max_tokens, target_mode=target_mode, clip_tau=clip_tau or 0.0)
-    return int(lib.ttt_mlp_workspace_bytes(C.byref(cfg)))
+    fn = {"all": lib.ttt_mlp_workspace_bytes, "state": lib.ttt_mlp_state_bytes,
+          "scratch": lib.ttt_mlp_scratch_bytes}[part]
+    return int(fn(C.byref(cfg)))
+
+
+def is_ttt_layer(layer: int, ttt_every: int) -> bool:
+    """Whether 0-based block `layer` carries In-Place TTT when every
+    `ttt_every`-th block does: the ttt_every-th, 2*ttt_every-th, ... blocks
+    (1-based), so ttt_every=1 makes every block a TTT block."""
+    return (layer + 1) % ttt_every == 0
 
 
 class TTTStack:
-    """Pre-norm residual stack of SwiGLU MLP blocks whose down projections are
-    In-Place TTT fast weights (no attention):
-        h_{l+1} = h_l + TTT_MLP_l(RMSNorm(h_l)),   X0 = h_0 for every layer.
-    Layer-major: each layer runs its chunk recursion over the whole call before
-    the next layer starts (the recursion is per layer and nothing else mixes
-    tokens).  All layers share one workspace, so a call processes whole
-    documents: its fast weights start at W_0 (doc_starts must contain 0) and
-    are not kept across calls.
+    """Pre-norm residual stack of SwiGLU MLP blocks (no attention):
+        h_{l+1} = h_l + MLP_l(RMSNorm(h_l)),   X0 = h_0 for every TTT block,
+    where MLP_l is an In-Place TTT block (fast W_down) when
+    is_ttt_layer(l, ttt_every) and the static SwiGLU MLP otherwise.
+    Layer-major: each block runs its chunk recursion over the whole call before
+    the next block starts (the recursion is per block and nothing else mixes
+    tokens).  Every block has its own handle, made once: its fast-weight state
+    is its own and the per-call scratch is shared (the blocks run one after
+    another on one stream).  A call processes whole documents: the fast
+    weights start at W_0 (doc_starts must contain 0).
 
     layers: list of dicts with CUDA tensors w_gate, w_up, w_down0, conv_w,
     w_target (one dtype).  h is fp32 (T x d); activations are cast to the
@@ -195,18 +232,25 @@ class TTTStack:
     """
 
     def __init__(self, layers, *, chunk: int, eta: float, max_tokens: int, eps: float = 1e-6,
-                 target_mode: int = _abi.TTT_TARGET_NEXT, clip_tau: float = 0.0):
+                 target_mode: int = _abi.TTT_TARGET_NEXT, clip_tau: float = 0.0,
+                 ttt_every: int = 1, stream=None):
+        if ttt_every < 1:
+            raise ValueError("ttt_every must be >= 1")
         self.layers = layers
         w = layers[0]
         self.dtype = w["w_gate"].dtype
         f, d = w["w_gate"].shape
         self.d, self.f, self.k = d, f, w["conv_w"].shape[0]
         self.chunk, self.eta, self.max_tokens, self.eps = chunk, eta, max_tokens, eps
-        self.target_mode, self.clip_tau = target_mode, clip_tau
+        self.target_mode, self.clip_tau, self.ttt_every = target_mode, clip_tau, ttt_every
         nbytes = workspace_bytes(d, f, chunk=chunk, conv_k=self.k, dtype=self.dtype,
                                  max_tokens=max_tokens, eta=eta, target_mode=target_mode,
-                                 clip_tau=clip_tau)
-        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=w["w_gate"].device)
+                                 clip_tau=clip_tau, part="scratch")
+        self.scratch = torch.empty(nbytes, dtype=torch.uint8, device=w["w_gate"].device)
+        self.blocks = [TTTMLP(lw["w_gate"], lw["w_up"], lw["w_down0"], lw["conv_w"], lw["w_target"],
+                              chunk=chunk, eta=eta, max_tokens=max_tokens, stream=stream,
+                              scratch=self.scratch, target_mode=target_mode, clip_tau=clip_tau)
+                       for lw in layers]
 
     def forward(self, h0: torch.Tensor, doc_starts: Sequence[int] = (0,), stream=None,
                 n_layers: Optional[int] = None) -> torch.Tensor:
@@ -218,19 +262,26 @@ class TTTStack:
         x0 = h0.to(self.dtype)
         x = torch.empty(h0.shape, dtype=self.dtype, device=h0.device)
         o = torch.empty_like(x)
-        for w in self.layers[: n_layers or len(self.layers)]:
+        n = n_layers or len(self.blocks)
+        for li, blk in enumerate(self.blocks[:n]):
             rmsnorm(h, x, self.eps, stream=stream)
-            layer = TTTMLP(w["w_gate"], w["w_up"], w["w_down0"], w["conv_w"], w["w_target"],
-                           chunk=self.chunk, eta=self.eta, max_tokens=self.max_tokens,
-                           stream=stream, workspace=self.workspace, target_mode=self.target_mode,
-                           clip_tau=self.clip_tau)
-            layer.forward(x, x0, doc_starts=doc_starts, out=o, stream=stream)
-            layer.check(stream=stream)
-            layer.close()
+            if is_ttt_layer(li, self.ttt_every):
+                blk.forward(x, x0, doc_starts=doc_starts, out=o, stream=stream)
+            else:
+                blk.forward_static(x, out=o, stream=stream)
             residual_add(h, o, stream=stream)
         return h
 
     __call__ = forward
+
+    def check(self, stream=None):
+        """Synchronise and raise if any block's in-kernel wait ran out."""
+        for blk in self.blocks:
+            blk.check(stream=stream)
+
+    def close(self):
+        for blk in self.blocks:
+            blk.close()
 
 
 def rmsnorm(h: torch.Tensor, out: torch.Tensor, eps: float = 1e-6, stream=None) -> torch.Tensor:

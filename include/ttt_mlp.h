@@ -114,6 +114,32 @@ ttt_status ttt_mlp_create(const ttt_mlp_config* cfg, const void* w_gate, const v
                           void* workspace, size_t workspace_bytes, void* stream,
                           ttt_mlp** out);
 
+/* The workspace in two parts, for several handles (for example the layers of
+ * a stack) that share one scratch buffer.  The state part holds what belongs
+ * to one handle across calls: a control block (the in-kernel error word and
+ * tile counters), the n_docs fast weights, their bf16 operand copies and the
+ * transposed W_target.  The scratch part holds what one forward call needs
+ * and leaves behind: Z, U, V, the intra-group Gram blocks and the
+ * host-staging buffers.  ttt_mlp_workspace_bytes(cfg) is the state part
+ * rounded up to 256 bytes plus the scratch part.  Both return 0 for an
+ * invalid configuration.  Host only; no CUDA call. */
+size_t ttt_mlp_state_bytes(const ttt_mlp_config* cfg);
+size_t ttt_mlp_scratch_bytes(const ttt_mlp_config* cfg);
+
+/* ttt_mlp_create with the two parts given separately: `state` of at least
+ * ttt_mlp_state_bytes(cfg) bytes and `scratch` of at least
+ * ttt_mlp_scratch_bytes(cfg) bytes, both device buffers, 256-byte aligned,
+ * not overlapping.  The state is the handle's alone; the scratch may be shared
+ * by handles whose configurations need no more than its size, provided their
+ * calls never overlap on the GPU (one stream, or ordered by the caller): a
+ * forward call overwrites the scratch, and ttt_mlp_intermediates() shows the
+ * last call of any handle that shares it.  Otherwise as ttt_mlp_create
+ * (which is this call with the workspace cut into its two parts). */
+ttt_status ttt_mlp_create_split(const ttt_mlp_config* cfg, const void* w_gate, const void* w_up,
+                                const void* w_down0, const void* conv_w, const void* w_target,
+                                void* state, size_t state_bytes, void* scratch,
+                                size_t scratch_bytes, void* stream, ttt_mlp** out);
+
 /* Run the layer over n_tokens tokens of document slot `doc`, continuing that
  * slot's fast weight.  x, x0: n_tokens x d device buffers (x0 may equal x);
  * o: n_tokens x d output (must not overlap x or x0).  doc_starts: host array
@@ -125,6 +151,16 @@ ttt_status ttt_mlp_create(const ttt_mlp_config* cfg, const void* w_gate, const v
 ttt_status ttt_mlp_forward_chunks(ttt_mlp* h, int32_t doc, const void* x, const void* x0,
                                   int64_t n_tokens, const int64_t* doc_starts,
                                   int32_t n_doc_starts, void* o, void* stream);
+
+/* The block's static MLP, o = SwiGLU(x) W_0^T = (SiLU(x W_gate^T) (.)
+ * (x W_up^T)) W_down^T, with the frozen W_down and no fast weight: the
+ * ordinary MLP block of the layers that do not carry In-Place TTT (the
+ * summary page's appendix C.3 puts TTT in every sixth MLP block; the others
+ * are unchanged), and what the layer computes with eta = 0.  x, o:
+ * n_tokens x d device buffers (o must not overlap x); 0 <= n_tokens <=
+ * max_tokens.  Uses the scratch part; reads and writes no fast weight. */
+ttt_status ttt_mlp_forward_static(ttt_mlp* h, const void* x, int64_t n_tokens, void* o,
+                                  void* stream);
 
 /* The same call with host buffers: x_host / x0_host are copied to device
  * staging inside the workspace, the layer runs, and O is copied back into
@@ -220,7 +256,9 @@ const char* ttt_mlp_path(const ttt_mlp* h);
  * overlap on the GPU (different streams, or different host threads) race and
  * must be serialised by the caller.  status: optional device int32 that
  * receives 0, or the code of an in-kernel wait that ran out (the output is
- * then incomplete); may be NULL. */
+ * then incomplete).  With status == NULL such a timeout is recorded only in
+ * the shared array, which the next call clears, so it cannot be detected:
+ * callers that need to know whether v is complete must pass status. */
 #define TTT_NOALLOC_SCRATCH_BYTES (32u << 20)
 ttt_status ttt_target_noalloc(const void* x0, const void* conv_w, const void* w_target,
                               int64_t n_tokens, int32_t d, int32_t conv_k, int32_t chunk,

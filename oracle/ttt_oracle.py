@@ -284,7 +284,8 @@ def static_mlp(x, w_gate, w_up, w_down) -> np.ndarray:
 
 
 def ttt_stack(h0, layers, eta, chunk, doc_starts=(0,), eps=1e-6, n_layers=None,
-              x0=None, target_mode=TARGET_NEXT, clip_tau=None, ttt_every=1):
+              x0=None, target_mode=TARGET_NEXT, clip_tau=None, ttt_every=1,
+              return_states=False):
     """Stack of pre-norm residual SwiGLU MLP blocks (no attention).
 
     h_{l+1} = h_l + MLP_l(RMSNorm(h_l)) with X0 = h_0 for every TTT block (X0
@@ -295,10 +296,12 @@ def ttt_stack(h0, layers, eta, chunk, doc_starts=(0,), eps=1e-6, n_layers=None,
     itself).  Each layer's recursion runs over all tokens before the next
     layer starts; that is the same computation because nothing mixes tokens
     across layers except the per-layer chunk recursion.  Returns (h_L, list of
-    the final W per layer; a static block's is its W_down)."""
+    the final W per layer; a static block's is its W_down), and with
+    ``return_states`` also the list h_0, h_1, ..., h_L."""
     h = _f64(h0).copy()
     x0 = _f64(h0 if x0 is None else x0)
     finals = []
+    states = [h.copy()]
     for li, w in enumerate(layers[: n_layers or len(layers)]):
         xn = rms_norm(h, eps)
         if (li + 1) % ttt_every == 0:
@@ -309,4 +312,6 @@ def ttt_stack(h0, layers, eta, chunk, doc_starts=(0,), eps=1e-6, n_layers=None,
             o, wf = static_mlp(xn, w["w_gate"], w["w_up"], w["w_down0"]), _f64(w["w_down0"])
         h = h + o
         finals.append(wf)
-    return h, finals
+        if return_states:
+            states.append(h.copy())
+    return (h, finals, states) if return_states else (h, finals)

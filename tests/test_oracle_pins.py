@@ -514,6 +514,22 @@ def test_stack_placement_matches_brute_force_composition(every):
     if every == 1:
         h1, _ = orc.ttt_stack(h0, layers, meta["eta"], meta["chunk"])
         assert np.array_equal(h, h1)
+    # the per-block states: h_0 = h0, h_L = the result, and each step is the
+    # block output of the brute-force composition above
+    _, _, states = orc.ttt_stack(h0, layers, meta["eta"], meta["chunk"], ttt_every=every,
+                                 return_states=True)
+    assert len(states) == len(layers) + 1
+    assert np.array_equal(states[0], np.float64(h0)) and np.array_equal(states[-1], h)
+    hb = np.float64(h0)
+    for li, w in enumerate(layers):
+        xn = F.rms_norm(_t(hb), (hb.shape[1],), eps=1e-6).numpy()
+        if (li + 1) % every == 0:
+            ob, _ = brute_force_layer(xn, h0, w["w_gate"], w["w_up"], w["w_down0"], w["conv_w"],
+                                      w["w_target"], meta["eta"], meta["chunk"])
+        else:
+            ob = _torch_static_mlp(xn, w["w_gate"], w["w_up"], w["w_down0"])
+        assert _rel(states[li + 1], hb + ob) < 1e-12
+        hb = hb + ob
 
 
 def test_static_mlp_matches_torch_and_eta_zero_layer():

@@ -325,6 +325,66 @@ def test_zero_conv_keeps_w0_bitwise_for_any_eta():
     assert _rel(_host(o), o_ref) < TOL_BF16
 
 
+@pytest.mark.parametrize("path,C", [("tcgen05", 64), ("tcgen05", 1024), ("simt", 64)])
+def test_static_forward_is_the_plain_mlp(path, C):
+    """ttt_mlp_forward_static: SwiGLU(X) W_0^T against the oracle's static
+    MLP, on both kernel families; and the same values as a forward call with
+    eta = 0 (whose updates add exact zeros)."""
+    cfg = _bf16_cfg(T=777, C=C, eta=0.0)
+    if path == "simt":
+        os.environ["TTT_FORCE_SIMT"] = "1"
+    try:
+        layer, dt = _make_gpu_layer(cfg)
+    finally:
+        os.environ.pop("TTT_FORCE_SIMT", None)
+    assert layer.path == path
+    x = _dev(cfg["x"], dt)
+    o = layer.forward_static(x)
+    o_eta0 = layer.forward(x)
+    w = layer.get_fast_weight()
+    layer.check()
+    ref = orc.static_mlp(cfg["x"], cfg["w_gate"], cfg["w_up"], cfg["w_down0"])
+    e = _rel(_host(o), ref)
+    e0 = _rel(_host(o), _host(o_eta0))
+    print(f"{path} C={C}: static O err {e:.3e}; vs the eta=0 layer {e0:.3e} "
+          f"(bitwise {torch.equal(o, o_eta0)})")
+    assert e <= TOL_BF16
+    assert e0 <= 1e-6
+    assert np.array_equal(_host(w), np.float64(cfg["w_down0"]))
+
+
+def test_handles_sharing_scratch_equal_private_workspaces():
+    """Two layers with their own state and one shared scratch, called one
+    after another on one stream (and interleaved across two calls each), give
+    the same bits as two layers with private workspaces."""
+    from chunk_wise_weight_ttt_b300 import TTTMLP, workspace_bytes
+    cfgs = [_bf16_cfg(T=900, C=64, seed=s, starts=(0, 300)) for s in (11, 12)]
+    dt = torch.bfloat16
+    scratch = torch.empty(workspace_bytes(256, 512, chunk=64, conv_k=5, max_tokens=900,
+                                          part="scratch"), dtype=torch.uint8, device="cuda")
+    shared, private = [], []
+    for cfg in cfgs:
+        ws = [_dev(cfg[k], dt) for k in ("w_gate", "w_up", "w_down0", "conv_w", "w_target")]
+        shared.append(TTTMLP(*ws, chunk=64, eta=cfg["eta"], max_tokens=900, scratch=scratch))
+        private.append(TTTMLP(*ws, chunk=64, eta=cfg["eta"], max_tokens=900))
+    xs = [_dev(cfg["x"], dt) for cfg in cfgs]
+    outs = {}
+    for rnd in range(2):
+        for i in range(2):
+            starts = (0, 300) if rnd == 0 else ()
+            outs[("s", rnd, i)] = shared[i].forward(xs[i], doc_starts=starts).clone()
+            outs[("p", rnd, i)] = private[i].forward(xs[i], doc_starts=starts)
+    for l in shared + private:
+        l.check()
+    for rnd in range(2):
+        for i in range(2):
+            assert torch.equal(outs[("s", rnd, i)], outs[("p", rnd, i)]), (rnd, i)
+    for i in range(2):
+        assert torch.equal(shared[i].get_fast_weight(), private[i].get_fast_weight())
+    o_ref, w_ref = _oracle(cfgs[0])
+    assert _rel(_host(outs[("s", 0, 0)]), o_ref) < TOL_BF16
+
+
 def test_state_persists_across_calls_and_reset():
     """Two calls (the second continues the document) equal the oracle run from
     the first call's final state; reset() restores W_0 exactly."""
