@@ -370,12 +370,26 @@ __global__ void to_f32_kernel(const T* __restrict__ src, float* __restrict__ dst
     dst[i] = to_f(src[i]);
 }
 
-// dst[i] = bf16(src[i])  (bf16 operand copy of the fp32 fast weight)
-__global__ void to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
-                               long long n) {
+// The fp32 fast weight as two 16-bit planes (tcgen05 path): hi = the upper
+// half of the bits rounded half up in magnitude, lo = the signed remainder,
+// so that (hi << 16) + lo is the value's bits exactly.
+__global__ void split_planes_kernel(const float* __restrict__ w, uint16_t* __restrict__ hi,
+                                    uint16_t* __restrict__ lo, long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint32_t b = __float_as_uint(w[i]);
+    const uint32_t h = (b + 0x8000u) >> 16;
+    hi[i] = static_cast<uint16_t>(h);
+    lo[i] = static_cast<uint16_t>(b - (h << 16));
+  }
+}
+
+__global__ void join_planes_kernel(const uint16_t* __restrict__ hi, const uint16_t* __restrict__ lo,
+                                   float* __restrict__ w, long long n) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x)
-    dst[i] = __float2bfloat16_rn(src[i]);
+    w[i] = __uint_as_float((static_cast<uint32_t>(hi[i]) << 16) +
+                           static_cast<uint32_t>(static_cast<int32_t>(static_cast<int16_t>(lo[i]))));
 }
 
 // out[c, r] = in[r, c] for an R x Cc matrix (32x32 tiles through shared memory).

@@ -41,13 +41,22 @@
 //            each group's tiles being its apply tiles
 //              O_g = Z_g W_s^T + S_g V_g            (W_s = state at group start)
 //            and its update tiles
-//              W <- W_s + V_g^T Z_g,  Wb_next <- bf16(W)
-//            in one launch.  An update tile accumulates V_g^T Z_g from zero
-//            in TMEM; its epilogue adds the fp32 block of W_s (or, at a
-//            document start, of W_0) in one rounding (read in a coalesced
-//            layout, one 32-column slice ahead, after the producer prefetched
-//            it into L2 at the tile's start) and stores W and its bf16 copy,
-//            coalesced through a per-warp shared-memory transpose.
+//              W <- W_s + V_g^T Z_g
+//            in one launch.  The fp32 state is kept as two 16-bit planes:
+//            hi, the upper half of W's bits rounded half up in magnitude (a
+//            bf16 value within half an ulp of W: the apply tiles' operand),
+//            and lo, the signed remainder, so (hi << 16) + lo is W's bits
+//            exactly.  hi is double-buffered (the apply tiles of a group read
+//            the plane that its update tiles do not write).  An update tile
+//            accumulates V_g^T Z_g from zero in TMEM; its epilogue rebuilds
+//            the fp32 block of W_s from hi and lo (or, at a document start,
+//            takes W_0), adds in one fp32 rounding (read in a coalesced
+//            layout, one 64-column slice ahead, after the producer prefetched
+//            both planes into L2 at the tile's start) and stores the new
+//            planes, coalesced through a per-warp shared-memory transpose.
+//            Against a separate fp32 state and bf16 copy this writes 4 bytes
+//            of state per element and group instead of 6, and the apply and
+//            update tiles read the same hi plane.
 //            Applying W_s to every chunk of the group plus the intra-group
 //            correction S_g V_g equals applying each chunk's own pre-update
 //            state (the deltas are additive, appendix B of the "In-Place
@@ -84,11 +93,9 @@ constexpr int kGemmThreads = 192;
 constexpr int kMaxGroups = 256;
 constexpr int kSwizzlePairs = 8;   // SwiGLU raster: tile pairs per column sweep
 constexpr uint16_t kPairMask = 0x3;  // both CTAs of the cluster
-// An update tile's fp32 W block, as L2-prefetch boxes of 32 columns x 128 rows.
-constexpr int kWBoxCols = 32;
-constexpr int kWBoxes = kBN / kWBoxCols;
-// per-warp staging for the transposed (coalesced) update-tile stores
-constexpr int kStgBytesPerWarp = 32 * 128;
+// per-warp staging for the transposed (coalesced) update-tile stores: 32 rows
+// of a 64-column fp32 slice
+constexpr int kStgBytesPerWarp = 32 * 256;
 constexpr int kEpiWarps = 4;
 
 enum GemmMode : int { kSwiGLU = 0, kLinear = 1, kSGram = 2, kGroup = 3, kDGram = 4 };
@@ -98,17 +105,17 @@ enum GemmMode : int { kSwiGLU = 0, kLinear = 1, kSGram = 2, kGroup = 3, kDGram =
 //   kLinear: 0 A (64x128), 1 B (64x128)
 //   kSGram:  0 Z (64x128), 1 Z (64x128)
 //   kDGram:  0 Z or V (64x128), 1 the same (64x128); `f` holds its width
-//   kGroup:  0 Z (64x128), 1 Wb[0] (64x128), 2 S (64x128),
+//   kGroup:  0 Z (64x128), 1 hi[0] of the slot (64x128), 2 S (64x128),
 //            3 V MN-major (64x64), 4 V MN-major with the run's K extent,
 //            5 Z MN-major (64x64) with the run's K extent,
-//            6 W fp32 of the slot (32 columns x 128 rows), 7 Wb[1] (64x128),
+//            6 lo of the slot (64x128, L2-prefetch boxes), 7 hi[1] (64x128),
 //            8 W_0 bf16 (64x128)
 constexpr int kNumMaps = 9;
 
 // kGroup per-group flags
 constexpr uint8_t kGrpReset = 1;  // document start: the group's state is W_0
-constexpr uint8_t kGrpInWb1 = 2;  // W_s is in Wb[1] (else Wb[0]; ignored with kGrpReset)
-constexpr uint8_t kGrpOutWb1 = 4; // the update tiles write bf16(W) to Wb[1] (else Wb[0])
+constexpr uint8_t kGrpInWb1 = 2;  // W_s's hi plane is hi[1] (else hi[0]; ignored with kGrpReset)
+constexpr uint8_t kGrpOutWb1 = 4; // the update tiles write the new hi plane to hi[1] (else hi[0])
 
 struct GemmArgs {
   CUtensorMap map[kNumMaps];
@@ -120,8 +127,8 @@ struct GemmArgs {
   int* counter;  // dynamic tile-pair counter, zero at launch
   int* err;      // workspace error word
   void* out0;    // kSwiGLU: Z; kLinear: V or O (n_rows x d); kSGram: S; kGroup: O
-  void* out1;    // kGroup: W (fp32, updated in place)
-  void* wb[2];   // kGroup: the two bf16 copies of the state (read / written alternately)
+  void* lo;      // kGroup: the lo plane of the slot's state (updated in place)
+  void* hi[2];   // kGroup: the slot's two hi planes (read / written alternately)
   const void* w0;  // kGroup: W_0 (bf16)
   // groups
   int s_pad;         // row/column pitch of one S block (multiple of 256)
@@ -326,12 +333,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // 16-byte global load cached in L2 only.
-__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
-  float4 v;
-  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+__device__ __forceinline__ uint4 ld_cg_u4(const uint16_t* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
+}
+
+// The two 16-bit planes of an fp32 value's bits b: hi = the upper half
+// rounded half up in magnitude (a bf16 within half an ulp of the value; b +
+// 0x8000 cannot carry into the sign for a finite value), lo = b - (hi << 16)
+// as a signed 16-bit remainder, in [-0x8000, 0x7fff].  join_hi_lo inverts
+// them exactly (the low 16 bits of its arguments are used).
+__device__ __forceinline__ uint32_t hi_of(uint32_t b) { return (b + 0x8000u) >> 16; }
+__device__ __forceinline__ uint32_t lo_of(uint32_t b, uint32_t h) { return (b - (h << 16)) & 0xFFFFu; }
+__device__ __forceinline__ uint32_t join_hi_lo(uint32_t h, uint32_t l) {
+  return ((h & 0xFFFFu) << 16) + static_cast<uint32_t>(static_cast<int32_t>(static_cast<int16_t>(l & 0xFFFFu)));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
@@ -387,70 +405,99 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
   } else if (MODE == kLinear || MODE == kGroup) {
     if (MODE == kGroup && ti.kind == 1) {
       // fast-weight update: W <- W_s + acc (acc = V^T Z of the group, from
-      // zero), one fp32 rounding.  Each 32-column slice of the warp's 32 rows
-      // goes TMEM -> registers (row per thread) -> staging (16-byte chunks
-      // XOR-swizzled by row, so both phases are bank-conflict free) -> the
-      // coalesced layout (4 full rows per instruction), where the thread adds
-      // W_s, read in that same layout one slice ahead, and stores W and its
-      // bf16 copy.
+      // zero), one fp32 rounding.  The warp's 32 rows go in four 64-column
+      // slices: TMEM -> registers (row per thread, 32 columns per load) ->
+      // staging (256-byte rows of 16-byte chunks, chunk q of row r at
+      // q ^ (r % 8): both phases bank-conflict free) -> the coalesced layout,
+      // where a thread owns 8 consecutive columns of a row, so that 8 lanes
+      // cover a row's 128 bytes of a plane and every global access of the warp
+      // is 4 whole lines.  There the thread rebuilds W_s from its hi and lo
+      // planes (read one slice ahead), adds, and stores the new planes.
       const int lane = row & 31;
       const int rbase = ti.m0 + (row - lane);
       const uint8_t fl = a.g_flags[ti.g];
       const bool from_w0 = fl & kGrpReset;
-      float* W = reinterpret_cast<float*>(a.out1);
-      const __nv_bfloat16* W0 = reinterpret_cast<const __nv_bfloat16*>(a.w0);
-      __nv_bfloat16* Wb = reinterpret_cast<__nv_bfloat16*>(a.wb[(fl & kGrpOutWb1) ? 1 : 0]);
-      const uint32_t st_row = smem_u32(stg) + lane * 128;
+      const uint16_t* HI = reinterpret_cast<const uint16_t*>(a.hi[(fl & kGrpInWb1) ? 1 : 0]);
+      uint16_t* HO = reinterpret_cast<uint16_t*>(a.hi[(fl & kGrpOutWb1) ? 1 : 0]);
+      uint16_t* LO = reinterpret_cast<uint16_t*>(a.lo);
+      const uint16_t* W0 = reinterpret_cast<const uint16_t*>(a.w0);
+      const uint32_t stg_u = smem_u32(stg);
+      const uint32_t st_row = stg_u + lane * 256;
       const int cq = lane & 7;
-      float4 wc[8], wn[8];
-      auto load_w = [&](int s, float4 (&dst)[8]) {
-        const int col = ti.n0 + s * 32 + cq * 4;
+      uint4 hc[8], lc[8], hn[8], ln[8];  // W_s planes, 8 columns per entry (rows 4j + lane / 8)
+      auto load_w = [&](int u, uint4 (&hd)[8], uint4 (&ld)[8]) {
+        const int col = ti.n0 + u * 64 + cq * 8;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int wr = rbase + j * 4 + (lane >> 3);
+          hd[j] = make_uint4(0u, 0u, 0u, 0u);
+          ld[j] = make_uint4(0u, 0u, 0u, 0u);
           if (wr < a.d && col < a.f) {
+            const size_t off = (size_t)wr * a.f + col;
             if (from_w0) {
-              const uint2 v = *reinterpret_cast<const uint2*>(W0 + (size_t)wr * a.f + col);
-              const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-              const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-              dst[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+              hd[j] = ld_cg_u4(W0 + off);
             } else {
-              dst[j] = ld_cg_f4(W + (size_t)wr * a.f + col);
+              hd[j] = ld_cg_u4(HI + off);
+              ld[j] = ld_cg_u4(LO + off);
             }
-          } else {
-            dst[j] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
       };
-      load_w(0, wc);
+      load_w(0, hc, lc);
 #pragma unroll
-      for (int s = 0; s < kBN / 32; ++s) {
-        if (s + 1 < kBN / 32) load_w(s + 1, wn);
-        tmem_ld32(tacc + s * 32, r);
-        tmem_ld_wait(r);
+      for (int u = 0; u < kBN / 64; ++u) {
+        if (u + 1 < kBN / 64) load_w(u + 1, hn, ln);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st_shared_v4(st_row + ((q ^ (lane & 7)) << 4), r[4 * q], r[4 * q + 1], r[4 * q + 2],
-                       r[4 * q + 3]);
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld32(tacc + u * 64 + half * 32, r);
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(st_row + (((half * 8 + q) ^ (lane & 7)) << 4), r[4 * q], r[4 * q + 1],
+                         r[4 * q + 2], r[4 * q + 3]);
+        }
         __syncwarp();
-        const int col = ti.n0 + s * 32 + cq * 4;
+        const int col = ti.n0 + u * 64 + cq * 8;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int rr = j * 4 + (lane >> 3);
-          uint32_t v[4];
-          ld_shared_v4(smem_u32(stg) + rr * 128 + ((cq ^ (rr & 7)) << 4), v);
+          uint32_t v[8];
+          {
+            uint32_t t0[4], t1[4];
+            ld_shared_v4(stg_u + rr * 256 + (((2 * cq) ^ (rr & 7)) << 4), t0);
+            ld_shared_v4(stg_u + rr * 256 + (((2 * cq + 1) ^ (rr & 7)) << 4), t1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[e] = t0[e];
+              v[4 + e] = t1[e];
+            }
+          }
           const int wr = rbase + rr;
           if (wr < a.d && col < a.f) {
-            const float4 w = make_float4(wc[j].x + __uint_as_float(v[0]), wc[j].y + __uint_as_float(v[1]),
-                                         wc[j].z + __uint_as_float(v[2]), wc[j].w + __uint_as_float(v[3]));
-            *reinterpret_cast<float4*>(W + (size_t)wr * a.f + col) = w;
-            *reinterpret_cast<uint2*>(Wb + (size_t)wr * a.f + col) =
-                make_uint2(pack_bf16x2(w.x, w.y), pack_bf16x2(w.z, w.w));
+            const uint32_t hw[4] = {hc[j].x, hc[j].y, hc[j].z, hc[j].w};
+            const uint32_t lw[4] = {lc[j].x, lc[j].y, lc[j].z, lc[j].w};
+            uint32_t ho[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t b0 = __float_as_uint(__uint_as_float(join_hi_lo(hw[e], lw[e])) +
+                                                  __uint_as_float(v[2 * e]));
+              const uint32_t b1 = __float_as_uint(__uint_as_float(join_hi_lo(hw[e] >> 16, lw[e] >> 16)) +
+                                                  __uint_as_float(v[2 * e + 1]));
+              const uint32_t h0 = hi_of(b0), h1 = hi_of(b1);
+              ho[e] = h0 | (h1 << 16);
+              lo[e] = lo_of(b0, h0) | (lo_of(b1, h1) << 16);
+            }
+            const size_t off = (size_t)wr * a.f + col;
+            *reinterpret_cast<uint4*>(HO + off) = make_uint4(ho[0], ho[1], ho[2], ho[3]);
+            *reinterpret_cast<uint4*>(LO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
         }
         __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) wc[j] = wn[j];
+        for (int j = 0; j < 8; ++j) {
+          hc[j] = hn[j];
+          lc[j] = ln[j];
+        }
       }
     } else {
       // plain bf16 store of alpha * acc (kLinear) or acc (kGroup apply)
@@ -632,11 +679,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         const TileInfo ti = decode_tile<MODE>(a, t, rank);
         if (!ti.valid) continue;
         if (MODE == kGroup && ti.kind == 1 && !(a.g_flags[ti.g] & kGrpReset)) {
-          // the epilogue adds this tile's fp32 W block after the MMAs; bring
-          // it into L2 now so those reads hit there (L2 is the point of
-          // coherence, so a prefetch ahead of the block's last writer is safe)
-          for (int b = 0; b < kWBoxes; ++b)
-            tma_prefetch_l2_2d(&a.map[6], ti.n0 + b * kWBoxCols, ti.m0);
+          // the epilogue adds this tile's block of W_s (both planes) after
+          // the MMAs; bring it into L2 now so those reads hit there (L2 is the
+          // point of coherence, so a prefetch ahead of the block's last
+          // writer is safe)
+          const CUtensorMap* mhi = (a.g_flags[ti.g] & kGrpInWb1) ? &a.map[7] : &a.map[1];
+          for (int b = 0; b < kBN / kBK; ++b) {
+            tma_prefetch_l2_2d(mhi, ti.n0 + b * kBK, ti.m0);
+            tma_prefetch_l2_2d(&a.map[6], ti.n0 + b * kBK, ti.m0);
+          }
         }
         const int nkb = ti.nkb1 + ti.nkb2;
 #pragma unroll 1

@@ -28,8 +28,9 @@ struct ttt_mlp {
   bool tc;
   int G, L, s_pad, s_slots, num_sms;
   int max_pairs;            // co-resident CTA pairs of the tcgen05 kernels
-  float* W;                 // n_docs x d x f
-  __nv_bfloat16* Wb[2];     // bf16 operand copies of the current state
+  float* W;                 // fp32 path: n_docs x d x f
+  uint16_t* Whi;            // tcgen05 path: n_docs x 2 x d x f hi planes of the fp32 state
+  uint16_t* Wlo;            // tcgen05 path: n_docs x d x f lo planes
   __nv_bfloat16* WtT;       // W_target transposed (out x in)
   void *Z, *U, *V;          // per-call intermediates (n x f, n x d, n x d)
   __nv_bfloat16* S;         // s_slots blocks of s_pad x s_pad
@@ -37,9 +38,8 @@ struct ttt_mlp {
   void *xs, *x0s, *os;      // host-staging copies of x, x0, o
   int* ctrl;                // [0] error word, [64..] tile counters
   int counter_next;
-  int wb_owner;             // slot whose state Wb[wb_cur] holds, -1 = none
-  int wb_cur;
-  CUtensorMap map_wg, map_wu, map_wtT, map_s, map_w0, map_wb[2];
+  std::vector<uint8_t> hcur;  // per slot: which of its two hi planes is current
+  CUtensorMap map_wg, map_wu, map_wtT, map_s, map_w0;
   std::string err;
   // benchmark phase timing
   bool profiling;
@@ -103,7 +103,7 @@ int group_tokens() {
 struct Layout {
   bool tc;
   int G, L, s_pad, s_slots;
-  size_t ctrl, W, Wb0, Wb1, WtT, state_total;              // state part
+  size_t ctrl, W, Whi, Wlo, WtT, state_total;               // state part
   size_t Z, U, V, S, GZ, GV, xs, x0s, os, scratch_total;    // scratch part
 };
 
@@ -148,9 +148,11 @@ Layout make_layout(const ttt_mlp_config& c, bool tc) {
     return at;
   };
   l.ctrl = take(kCtrlInts * sizeof(int));
-  l.W = take((size_t)c.n_docs * d * f * 4);
-  l.Wb0 = tc ? take(d * f * 2) : 0;
-  l.Wb1 = tc ? take(d * f * 2) : 0;
+  // the fp32 state: fp32 values on the fp32 path; two hi planes and a lo
+  // plane (16 bits each) per slot on the tcgen05 path
+  l.W = tc ? 0 : take((size_t)c.n_docs * d * f * 4);
+  l.Whi = tc ? take((size_t)c.n_docs * 2 * d * f * 2) : 0;
+  l.Wlo = tc ? take((size_t)c.n_docs * d * f * 2) : 0;
   l.WtT = tc ? take(d * d * 2) : 0;
   l.state_total = o;
   o = 0;
@@ -481,9 +483,13 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
   h->prof_launches++;
 
   const size_t wsz = (size_t)d * f;
-  float* W = h->W + (size_t)doc * wsz;
-  CUtensorMap map_wf;  // the slot's fp32 fast weight, update-tile preload boxes
-  if (!make_map(&map_wf, W, f, d, f, 32, 128, &why, /*f32=*/true)) return fail(h, TTT_ECUDA, why);
+  uint16_t* hi[2] = {h->Whi + (size_t)doc * 2 * wsz, h->Whi + (size_t)doc * 2 * wsz + wsz};
+  uint16_t* lo = h->Wlo + (size_t)doc * wsz;
+  CUtensorMap map_hi[2], map_lo;  // the slot's state planes (operand / L2-prefetch boxes)
+  if (!make_map(&map_hi[0], hi[0], f, d, f, 64, 128, &why) ||
+      !make_map(&map_hi[1], hi[1], f, d, f, 64, 128, &why) ||
+      !make_map(&map_lo, lo, f, d, f, 64, 128, &why))
+    return fail(h, TTT_ECUDA, why);
   for (size_t w0 = 0; w0 < groups.size(); w0 += (size_t)h->s_slots) {
     const size_t w1 = std::min(groups.size(), w0 + (size_t)h->s_slots);
     // intra-group Gram blocks S_g = mask(Z_g Z_g^T) of this wave
@@ -554,20 +560,13 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
     for (size_t i = w0; i < w1;) {
       size_t e = i;  // the run's last group
       while (exact(e) && e + 1 < w1 && (int)(e + 1 - i) < run_max) ++e;
-      if (!groups[i].reset && h->wb_owner != doc) {
-        // the bf16 copy of the state belongs to another slot
-        to_bf16_kernel<<<grid_for((long long)wsz, 256), 256, 0, st>>>(W, h->Wb[h->wb_cur], (long long)wsz);
-        TTT_CK_LAUNCH(h);
-        h->prof_launches++;
-        h->wb_owner = doc;
-      }
       GemmArgs& q = a;
       q.map[0] = map_za;
-      q.map[1] = h->map_wb[0];
+      q.map[1] = map_hi[0];
       q.map[2] = h->map_s;
       q.map[3] = map_vmn;
-      q.map[6] = map_wf;
-      q.map[7] = h->map_wb[1];
+      q.map[6] = map_lo;
+      q.map[7] = map_hi[1];
       q.map[8] = h->map_w0;
       if (exact(e)) {
         q.map[4] = map_vmn;
@@ -579,10 +578,10 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
           return fail(h, TTT_ECUDA, why);
       }
       // per group: its tiles, where its state comes from (W_0 at a document
-      // start, else the bf16 copy the previous group wrote) and where its
-      // update tiles write the next copy
+      // start, else the hi plane the previous group wrote) and where its
+      // update tiles write the next hi plane
       q.n_groups = (int)(e - i + 1);
-      int cur = h->wb_cur, tiles = 0;
+      int cur = h->hcur[doc], tiles = 0;
       for (int k = 0; k < q.n_groups; ++k) {
         const Span& g = groups[i + k];
         q.g_start[k] = g.start;
@@ -601,9 +600,9 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
       q.g_tile[q.n_groups] = tiles;
       q.slot0 = (int)(i - w0);
       q.out0 = o;
-      q.out1 = W;
-      q.wb[0] = h->Wb[0];
-      q.wb[1] = h->Wb[1];
+      q.lo = lo;
+      q.hi[0] = hi[0];
+      q.hi[1] = hi[1];
       q.w0 = h->w0;
       int* ctr = next_counters(h, st, 1 + 2 * q.n_groups * npd);
       q.counter = ctr;
@@ -611,8 +610,7 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
       TTT_CK(h, launch_gemm<kGroup>(h, q, tiles, st));
       h->prof_launches++;
       h->prof_group_launches++;
-      h->wb_cur = cur;
-      h->wb_owner = doc;
+      h->hcur[doc] = (uint8_t)cur;
       i = e + 1;
     }
     pt.end();
@@ -747,7 +745,6 @@ ttt_status forward_simt_t(ttt_mlp* h, int doc, const void* xv, const void* x0v, 
     TTT_CK_LAUNCH(h);
     h->prof_launches += 2;
   }
-  h->wb_owner = -1;
   return TTT_OK;
 }
 
@@ -823,13 +820,19 @@ std::vector<int64_t> host_cuts(ttt_mlp* h, int64_t n, const int64_t* ds, int nds
 
 ttt_status reset_slot(ttt_mlp* h, int doc, cudaStream_t st) {
   const size_t wsz = (size_t)h->cfg.d * h->cfg.f;
+  if (h->tc) {
+    // W_0 is bf16: its hi plane is W_0's bits and its lo plane is zero
+    TTT_CK(h, cudaMemcpyAsync(h->Whi + (size_t)doc * 2 * wsz + h->hcur[doc] * wsz, h->w0, wsz * 2,
+                              cudaMemcpyDeviceToDevice, st));
+    TTT_CK(h, cudaMemsetAsync(h->Wlo + (size_t)doc * wsz, 0, wsz * 2, st));
+    return TTT_OK;
+  }
   float* W = h->W + (size_t)doc * wsz;
   if (h->cfg.act_dtype == TTT_BF16)
     to_f32_kernel<__nv_bfloat16><<<grid_for((long long)wsz, 256), 256, 0, st>>>((const __nv_bfloat16*)h->w0, W, (long long)wsz);
   else
     to_f32_kernel<float><<<grid_for((long long)wsz, 256), 256, 0, st>>>((const float*)h->w0, W, (long long)wsz);
   TTT_CK_LAUNCH(h);
-  if (h->wb_owner == doc) h->wb_owner = -1;
   return TTT_OK;
 }
 
@@ -899,9 +902,10 @@ ttt_status ttt_mlp_create_split(const ttt_mlp_config* cfg, const void* w_gate, c
   uint8_t* sb = (uint8_t*)state;
   uint8_t* xb = (uint8_t*)scratch;
   h->ctrl = (int*)(sb + l.ctrl);
-  h->W = (float*)(sb + l.W);
-  h->Wb[0] = (__nv_bfloat16*)(sb + l.Wb0);
-  h->Wb[1] = (__nv_bfloat16*)(sb + l.Wb1);
+  h->W = tc ? nullptr : (float*)(sb + l.W);
+  h->Whi = tc ? (uint16_t*)(sb + l.Whi) : nullptr;
+  h->Wlo = tc ? (uint16_t*)(sb + l.Wlo) : nullptr;
+  h->hcur.assign((size_t)cfg->n_docs, 0);
   h->WtT = (__nv_bfloat16*)(sb + l.WtT);
   h->Z = xb + l.Z;
   h->U = xb + l.U;
@@ -913,8 +917,6 @@ ttt_status ttt_mlp_create_split(const ttt_mlp_config* cfg, const void* w_gate, c
   h->x0s = xb + l.x0s;
   h->os = xb + l.os;
   h->counter_next = kCounterBase;
-  h->wb_owner = -1;
-  h->wb_cur = 0;
   cudaStream_t st = (cudaStream_t)stream;
 
   int dev = 0;
@@ -935,9 +937,7 @@ ttt_status ttt_mlp_create_split(const ttt_mlp_config* cfg, const void* w_gate, c
         !make_map(&h->map_wu, w_up, d, f, d, 64, 128, &why) ||
         !make_map(&h->map_wtT, h->WtT, d, d, d, 64, 128, &why) ||
         !make_map(&h->map_s, h->S, h->s_pad, (uint64_t)h->s_slots * h->s_pad, h->s_pad, 64, 128, &why) ||
-        !make_map(&h->map_w0, w_down0, f, d, f, 64, 128, &why) ||
-        !make_map(&h->map_wb[0], h->Wb[0], f, d, f, 64, 128, &why) ||
-        !make_map(&h->map_wb[1], h->Wb[1], f, d, f, 64, 128, &why))
+        !make_map(&h->map_w0, w_down0, f, d, f, 64, 128, &why))
       return bail(TTT_ECUDA, why);
     e = setup_tc_kernels(&h->max_pairs);
     if (e != cudaSuccess)
@@ -1075,7 +1075,14 @@ ttt_status ttt_mlp_get_fast_weight(ttt_mlp* h, int32_t doc, float* dst, void* st
   if (doc < 0 || doc >= h->cfg.n_docs) return fail(h, TTT_EINVAL, "doc slot out of range");
   if (!dst) return fail(h, TTT_EINVAL, "dst is NULL");
   const size_t wsz = (size_t)h->cfg.d * h->cfg.f;
-  TTT_CK(h, cudaMemcpyAsync(dst, h->W + (size_t)doc * wsz, wsz * 4, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+  cudaStream_t st = (cudaStream_t)stream;
+  if (h->tc) {
+    join_planes_kernel<<<grid_for((long long)wsz, 256), 256, 0, st>>>(
+        h->Whi + (size_t)doc * 2 * wsz + h->hcur[doc] * wsz, h->Wlo + (size_t)doc * wsz, dst, (long long)wsz);
+    TTT_CK_LAUNCH(h);
+    return TTT_OK;
+  }
+  TTT_CK(h, cudaMemcpyAsync(dst, h->W + (size_t)doc * wsz, wsz * 4, cudaMemcpyDeviceToDevice, st));
   return TTT_OK;
 }
 
@@ -1085,8 +1092,14 @@ ttt_status ttt_mlp_set_fast_weight(ttt_mlp* h, int32_t doc, const float* src, vo
   if (doc < 0 || doc >= h->cfg.n_docs) return fail(h, TTT_EINVAL, "doc slot out of range");
   if (!src) return fail(h, TTT_EINVAL, "src is NULL");
   const size_t wsz = (size_t)h->cfg.d * h->cfg.f;
-  TTT_CK(h, cudaMemcpyAsync(h->W + (size_t)doc * wsz, src, wsz * 4, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
-  if (h->wb_owner == doc) h->wb_owner = -1;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (h->tc) {
+    split_planes_kernel<<<grid_for((long long)wsz, 256), 256, 0, st>>>(
+        src, h->Whi + (size_t)doc * 2 * wsz + h->hcur[doc] * wsz, h->Wlo + (size_t)doc * wsz, (long long)wsz);
+    TTT_CK_LAUNCH(h);
+    return TTT_OK;
+  }
+  TTT_CK(h, cudaMemcpyAsync(h->W + (size_t)doc * wsz, src, wsz * 4, cudaMemcpyDeviceToDevice, st));
   return TTT_OK;
 }
 

@@ -97,10 +97,12 @@ typedef struct {
 typedef struct ttt_mlp ttt_mlp; /* opaque handle */
 
 /* Bytes of device workspace a handle with this configuration needs (0 if the
- * configuration is invalid).  The workspace holds the n_docs fast weights,
- * their bf16 operand copies, the per-call intermediates (Z, U, V, the
- * intra-group Gram blocks), host-staging buffers and a small control area.
- * Host only; no CUDA call. */
+ * configuration is invalid).  The workspace holds the n_docs fast weights
+ * (fp32 values; on the tcgen05 path each is kept as two 16-bit planes, the
+ * upper half of its bits rounded half up in magnitude -- the bf16 operand of
+ * the apply -- twice, and the exact signed remainder), the per-call
+ * intermediates (Z, U, V, the intra-group Gram blocks), host-staging buffers
+ * and a small control area.  Host only; no CUDA call. */
 size_t ttt_mlp_workspace_bytes(const ttt_mlp_config* cfg);
 
 /* Create a handle.  The five weight pointers are device buffers of act_dtype
@@ -117,8 +119,7 @@ ttt_status ttt_mlp_create(const ttt_mlp_config* cfg, const void* w_gate, const v
 /* The workspace in two parts, for several handles (for example the layers of
  * a stack) that share one scratch buffer.  The state part holds what belongs
  * to one handle across calls: a control block (the in-kernel error word and
- * tile counters), the n_docs fast weights, their bf16 operand copies and the
- * transposed W_target.  The scratch part holds what one forward call needs
+ * tile counters), the n_docs fast weights and the transposed W_target.  The scratch part holds what one forward call needs
  * and leaves behind: Z, U, V, the intra-group Gram blocks and the
  * host-staging buffers.  ttt_mlp_workspace_bytes(cfg) is the state part
  * rounded up to 256 bytes plus the scratch part.  Both return 0 for an
@@ -185,7 +186,8 @@ ttt_status ttt_mlp_forward_chunks_host(ttt_mlp* h, int32_t doc, const void* x_ho
  * boundary, appendix B of the summary page). */
 ttt_status ttt_mlp_reset(ttt_mlp* h, int32_t doc, void* stream);
 
-/* Copy slot `doc`'s fp32 fast weight (d x f) to / from a device buffer. */
+/* Copy slot `doc`'s fp32 fast weight (d x f) to / from a device buffer.  Every
+ * fp32 bit pattern goes through unchanged. */
 ttt_status ttt_mlp_get_fast_weight(ttt_mlp* h, int32_t doc, float* dst, void* stream);
 ttt_status ttt_mlp_set_fast_weight(ttt_mlp* h, int32_t doc, const float* src, void* stream);
 

@@ -404,6 +404,35 @@ def test_state_persists_across_calls_and_reset():
     assert np.array_equal(_host(layer.get_fast_weight()), np.float64(cfg["w_down0"]))
 
 
+@pytest.mark.parametrize("path", ["tcgen05", "simt"])
+def test_fast_weight_round_trip_is_exact(path):
+    """set_fast_weight then get_fast_weight gives back every fp32 bit pattern,
+    on the tcgen05 path (where the state is kept as a hi and a lo 16-bit
+    plane) as on the fp32 one: ordinary values, both signs, values whose low
+    16 bits are exactly half way (0x8000) or just below, subnormals, zero."""
+    cfg = _bf16_cfg(d=256, f=512, T=64, C=64)
+    if path == "simt":
+        os.environ["TTT_FORCE_SIMT"] = "1"
+    try:
+        layer, _ = _make_gpu_layer(cfg)
+    finally:
+        os.environ.pop("TTT_FORCE_SIMT", None)
+    assert layer.path == path
+    rng = np.random.default_rng(5)
+    bits = rng.integers(0, 2 ** 32, size=(256, 512), dtype=np.uint64).astype(np.uint32)
+    bits &= np.uint32(0xBFFFFFFF)                     # finite: exponent below all-ones
+    bits[0, :64] = (bits[0, :64] & np.uint32(0xFFFF0000)) | np.uint32(0x8000)
+    bits[1, :64] = (bits[1, :64] & np.uint32(0xFFFF0000)) | np.uint32(0x7FFF)
+    bits[2, :64] = bits[2, :64] & np.uint32(0x807FFFFF)  # subnormals
+    bits[3, :8] = np.array([0, 0x80000000, 0x00008000, 0x80008000, 0x3F808000, 0xBF808000,
+                            0x7F7FFFFF, 0xFF7F7FFF], dtype=np.uint32)
+    w = torch.from_numpy(bits.view(np.float32)).cuda()
+    layer.set_fast_weight(w)
+    back = layer.get_fast_weight()
+    torch.cuda.synchronize()
+    assert np.array_equal(back.cpu().numpy().view(np.uint32), bits)
+
+
 def test_set_fast_weight_then_continue():
     cfg = _bf16_cfg(T=512, C=64)
     layer, dt = _make_gpu_layer(cfg)
