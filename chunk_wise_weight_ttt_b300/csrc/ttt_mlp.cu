@@ -36,6 +36,13 @@ struct ttt_mlp {
   __nv_bfloat16* S;         // s_slots blocks of s_pad x s_pad
   float *GZ, *GV;           // same-chunk Gram blocks for update clipping (or null)
   void *xs, *x0s, *os;      // host-staging copies of x, x0, o
+  // A handle that owns its scratch has two staging buffers for x and x0 and
+  // alternates them between host-buffer calls, so that a call's input copies
+  // can run while the previous call's layers do.
+  bool owns_scratch = false;
+  void *xs2 = nullptr, *x0s2 = nullptr;
+  int stage_sel = 0;
+  cudaEvent_t ev_free[2] = {nullptr, nullptr};  // the layers that read staging buffer b are done
   int* ctrl;                // [0] error word, [64..] tile counters
   int counter_next;
   std::vector<uint8_t> hcur;  // per slot: which of its two hi planes is current
@@ -54,7 +61,7 @@ struct ttt_mlp {
   cudaStream_t st_in = nullptr, st_out = nullptr;
   cudaEvent_t ev_start = nullptr, ev_in = nullptr, ev_out = nullptr;
   ~ttt_mlp() {
-    for (cudaEvent_t e : {ev_start, ev_in, ev_out})
+    for (cudaEvent_t e : {ev_start, ev_in, ev_out, ev_free[0], ev_free[1]})
       if (e) cudaEventDestroy(e);
     for (cudaStream_t q : {st_in, st_out})
       if (q) cudaStreamDestroy(q);
@@ -104,7 +111,7 @@ struct Layout {
   bool tc;
   int G, L, s_pad, s_slots;
   size_t ctrl, W, Whi, Wlo, WtT, state_total;               // state part
-  size_t Z, U, V, S, GZ, GV, xs, x0s, os, scratch_total;    // scratch part
+  size_t Z, U, V, S, GZ, GV, xs, x0s, os, xs2, x0s2, scratch_total;  // scratch part
 };
 
 bool config_ok(const ttt_mlp_config* c, std::string* why) {
@@ -170,6 +177,8 @@ Layout make_layout(const ttt_mlp_config& c, bool tc) {
   l.xs = take(n * d * act);
   l.x0s = take(n * d * act);
   l.os = take(n * d * act);
+  l.xs2 = take(n * d * act);
+  l.x0s2 = take(n * d * act);
   l.scratch_total = o;
   return l;
 }
@@ -916,6 +925,8 @@ ttt_status ttt_mlp_create_split(const ttt_mlp_config* cfg, const void* w_gate, c
   h->xs = xb + l.xs;
   h->x0s = xb + l.x0s;
   h->os = xb + l.os;
+  h->xs2 = xb + l.xs2;
+  h->x0s2 = xb + l.x0s2;
   h->counter_next = kCounterBase;
   cudaStream_t st = (cudaStream_t)stream;
 
@@ -974,8 +985,10 @@ ttt_status ttt_mlp_create(const ttt_mlp_config* cfg, const void* w_gate, const v
   // the workspace is the state part followed by the scratch part
   const size_t sb = align_up(state_bytes_of(*cfg), 256), xb = scratch_bytes_of(*cfg);
   if (workspace_bytes < sb + xb) return fail(nullptr, TTT_EINVAL, "workspace is smaller than ttt_mlp_workspace_bytes()");
-  return ttt_mlp_create_split(cfg, w_gate, w_up, w_down0, conv_w, w_target, workspace, sb,
-                              (uint8_t*)workspace + sb, workspace_bytes - sb, stream, out);
+  ttt_status r = ttt_mlp_create_split(cfg, w_gate, w_up, w_down0, conv_w, w_target, workspace, sb,
+                                      (uint8_t*)workspace + sb, workspace_bytes - sb, stream, out);
+  if (r == TTT_OK) (*out)->owns_scratch = true;
+  return r;
 }
 
 ttt_status ttt_mlp_forward_chunks(ttt_mlp* h, int32_t doc, const void* x, const void* x0,
@@ -1013,29 +1026,48 @@ ttt_status ttt_mlp_forward_chunks_host(ttt_mlp* h, int32_t doc, const void* x_ho
   if (!h->st_in) {
     TTT_CK(h, cudaStreamCreateWithFlags(&h->st_in, cudaStreamNonBlocking));
     TTT_CK(h, cudaStreamCreateWithFlags(&h->st_out, cudaStreamNonBlocking));
-    for (cudaEvent_t* e : {&h->ev_start, &h->ev_in, &h->ev_out})
+    for (cudaEvent_t* e : {&h->ev_start, &h->ev_in, &h->ev_out, &h->ev_free[0], &h->ev_free[1]})
       TTT_CK(h, cudaEventCreateWithFlags(e, cudaEventDisableTiming));
   }
   // Segments pipelined over three streams: segment k+1's input copy (st_in)
   // and segment k-1's output copy (st_out) overlap segment k's layer on
-  // `stream`.  Events order them; both copy streams first wait for
-  // everything already on `stream` (an earlier call may still read the
-  // staging buffers), and `stream` finally waits for the last output copy.
+  // `stream`.  Events order them, and `stream` finally waits for the last
+  // output copy.  The output copies first wait for everything already on
+  // `stream`.  The input copies wait only until the staging buffers they
+  // fill are free: with a scratch of its own the handle alternates two pairs
+  // of them between calls, so a call's input copies need only the layers of
+  // the call before the previous one to be done and overlap the previous
+  // call; with a shared scratch they wait for everything already on `stream`.
   const size_t tok = (size_t)h->cfg.d * (h->cfg.act_dtype == TTT_BF16 ? 2 : 4);
   const bool sep_x0 = x0_host != x_host;
+  const int buf = h->owns_scratch ? h->stage_sel : 0;
+  void* xs = buf ? h->xs2 : h->xs;
+  void* x0s = buf ? h->x0s2 : h->x0s;
   const std::vector<int64_t> cuts = host_cuts(h, n_tokens, doc_starts, n_doc_starts);
   auto copy_in = [&](size_t k) -> ttt_status {
     const size_t off = (size_t)cuts[k] * tok, len = (size_t)(cuts[k + 1] - cuts[k]) * tok;
-    TTT_CK(h, cudaMemcpyAsync((char*)h->xs + off, (const char*)x_host + off, len, cudaMemcpyHostToDevice, h->st_in));
+    TTT_CK(h, cudaMemcpyAsync((char*)xs + off, (const char*)x_host + off, len, cudaMemcpyHostToDevice, h->st_in));
     if (sep_x0)
-      TTT_CK(h, cudaMemcpyAsync((char*)h->x0s + off, (const char*)x0_host + off, len, cudaMemcpyHostToDevice,
+      TTT_CK(h, cudaMemcpyAsync((char*)x0s + off, (const char*)x0_host + off, len, cudaMemcpyHostToDevice,
                                 h->st_in));
     TTT_CK(h, cudaEventRecord(h->ev_in, h->st_in));
     return TTT_OK;
   };
   TTT_CK(h, cudaEventRecord(h->ev_start, st));
-  TTT_CK(h, cudaStreamWaitEvent(h->st_in, h->ev_start, 0));
+  TTT_CK(h, cudaStreamWaitEvent(h->st_in, h->owns_scratch ? h->ev_free[buf] : h->ev_start, 0));
   TTT_CK(h, cudaStreamWaitEvent(h->st_out, h->ev_start, 0));
+  // On any return from here on, mark the staging buffers as read by what
+  // this call has enqueued on `stream`, so that a later call never fills them
+  // under layers still in flight.
+  struct MarkFree {
+    ttt_mlp* h;
+    int buf;
+    cudaStream_t st;
+    bool armed = true;
+    ~MarkFree() {
+      if (armed) cudaEventRecord(h->ev_free[buf], st);
+    }
+  } mark{h, buf, st};
   if ((s = copy_in(0)) != TTT_OK) return s;
   for (size_t k = 0; k + 1 < cuts.size(); ++k) {
     const int64_t b = cuts[k], e = cuts[k + 1];
@@ -1045,7 +1077,7 @@ ttt_status ttt_mlp_forward_chunks_host(ttt_mlp* h, int32_t doc, const void* x_ho
     for (int i = 0; i < n_doc_starts; ++i)
       if (doc_starts[i] >= b && doc_starts[i] < e) dsk.push_back(doc_starts[i] - b);
     const size_t off = (size_t)b * tok;
-    s = forward_impl(h, doc, (char*)h->xs + off, (char*)(sep_x0 ? h->x0s : h->xs) + off, e - b, dsk.data(),
+    s = forward_impl(h, doc, (char*)xs + off, (char*)(sep_x0 ? x0s : xs) + off, e - b, dsk.data(),
                      (int)dsk.size(), (char*)h->os + off, st);
     if (s != TTT_OK) return s;
     TTT_CK(h, cudaEventRecord(h->ev_out, st));
@@ -1053,6 +1085,10 @@ ttt_status ttt_mlp_forward_chunks_host(ttt_mlp* h, int32_t doc, const void* x_ho
     TTT_CK(h, cudaMemcpyAsync((char*)o_host + off, (char*)h->os + off, (size_t)(e - b) * tok,
                               cudaMemcpyDeviceToHost, h->st_out));
   }
+  // the layers that read this call's staging buffers are enqueued
+  mark.armed = false;
+  TTT_CK(h, cudaEventRecord(h->ev_free[buf], st));
+  if (h->owns_scratch) h->stage_sel ^= 1;
   TTT_CK(h, cudaEventRecord(h->ev_out, h->st_out));
   TTT_CK(h, cudaStreamWaitEvent(st, h->ev_out, 0));
   return TTT_OK;

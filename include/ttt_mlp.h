@@ -168,9 +168,16 @@ ttt_status ttt_mlp_forward_static(ttt_mlp* h, const void* x, int64_t n_tokens, v
  * o_host.  The call is cut at group starts into segments of about 4096 tokens
  * (TTT_HOST_SEGMENT overrides), which give the same bits as one call; segment
  * k+1's input copy and segment k-1's output copy run on two copy streams of
- * the handle while segment k runs on `stream`.  The copies start after
+ * the handle while segment k runs on `stream`.  The output copies start after
  * everything already enqueued on `stream`, and `stream` waits for the last
- * one, so stream order is as if everything ran on `stream`.  Pinned
+ * one.  The input copies of a handle made by ttt_mlp_create (which owns its
+ * scratch) go to one of two staging buffers that alternate between calls, so
+ * they may start while the handle's previous call still runs: they wait only
+ * for the layers of the call before that, which read the same buffer.  A
+ * handle made by ttt_mlp_create_split (whose scratch may be shared) starts
+ * them after everything already enqueued on `stream`.  Either way x_host is
+ * read asynchronously and the results are as if everything ran on `stream`.
+ * Pinned
  * (page-locked) host buffers make the copies asynchronous and let them
  * overlap; the call returns once everything is enqueued, so the caller must
  * synchronise `stream` before reading o_host or reusing x_host.  If the call

@@ -491,6 +491,39 @@ def test_host_buffer_segments_equal_device_call():
     assert torch.equal(host_layer.get_fast_weight(), w_dev)
 
 
+def test_back_to_back_host_calls_with_prefetched_inputs():
+    """Four host-buffer calls in a row without synchronising, on different
+    documents (a handle that owns its scratch lets each call's input copies
+    overlap the previous call's layers, alternating two staging buffers), the
+    second and fourth continuing the state of the call before: every output
+    and the final state equal the device-buffer calls bit for bit.  A handle
+    on a shared scratch (no overlap of input copies) gives the same bits."""
+    from chunk_wise_weight_ttt_b300 import TTTMLP, workspace_bytes
+    cfg = make_layer(256, 512, 9000, 64, 4, 0.5, dtype="bf16", seed=8, init="qwen")
+    dt = torch.bfloat16
+    xs = [_dev(cfg["x"], dt)]
+    for k in range(1, 4):
+        xs.append((xs[0].float() * (1.0 - 0.2 * k) + 0.01 * k).to(dt))
+    starts = [(0,), (), (0, 4000), ()]
+    dev_layer, _ = _make_gpu_layer(cfg)
+    o_dev = [dev_layer.forward(x, doc_starts=ds) for x, ds in zip(xs, starts)]
+    w_dev = dev_layer.get_fast_weight()
+    dev_layer.check()
+    ws = [_dev(cfg[k], dt) for k in ("w_gate", "w_up", "w_down0", "conv_w", "w_target")]
+    scratch = torch.empty(workspace_bytes(256, 512, chunk=64, conv_k=4, max_tokens=9000,
+                                          part="scratch"), dtype=torch.uint8, device="cuda")
+    for layer in (TTTMLP(*ws, chunk=64, eta=cfg["eta"], max_tokens=9000),
+                  TTTMLP(*ws, chunk=64, eta=cfg["eta"], max_tokens=9000, scratch=scratch)):
+        xh = [x.cpu().pin_memory() for x in xs]
+        oh = [torch.empty_like(h).pin_memory() for h in xh]
+        for h, o, ds in zip(xh, oh, starts):
+            layer.forward_host(h, out_host=o, doc_starts=ds)
+        layer.check()
+        for k in range(4):
+            assert torch.equal(oh[k], o_dev[k].cpu()), k
+        assert torch.equal(layer.get_fast_weight(), w_dev)
+
+
 def test_bad_call_arguments_change_nothing():
     from chunk_wise_weight_ttt_b300 import TTTError
     cfg = _bf16_cfg(T=256, C=64)
