@@ -91,7 +91,11 @@ constexpr int kTmemCols = 2 * kBN;              // two fp32 accumulators
 constexpr int kSchedRing = 4;
 constexpr int kGemmThreads = 192;
 constexpr int kMaxGroups = 256;
-constexpr int kSwizzlePairs = 8;   // SwiGLU raster: tile pairs per column sweep
+// SwiGLU raster: tile pairs (of 256 token rows) per column sweep.  One sweep
+// streams all of W_gate and W_up (100 MB at the Qwen3-4B shape) while its X
+// rows (32 x 256 tokens: 42 MB) stay in L2; measured against sweeps of 8, 16,
+// 24 and 48 pairs, 32 gave the fastest step.
+constexpr int kSwizzlePairs = 32;
 constexpr uint16_t kPairMask = 0x3;  // both CTAs of the cluster
 // per-warp staging for the transposed (coalesced) update-tile stores: 32 rows
 // of a 64-column fp32 slice
