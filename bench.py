@@ -584,17 +584,24 @@ def run_extra(args):
                   "layer_tokens_per_s": c["n_layers"] * c["T"] / sec})
             stack.close()
             del stack
-        # the single TTT layer on the same shape, for the per-layer comparison
+        # the single TTT layer on the same shape, for the per-layer comparison:
+        # a step is as many calls as the stack has layers, so that both run
+        # for as long and under the same power-cap clock
         w = layers[0]
         single = TTTMLP(w["w_gate"], w["w_up"], w["w_down0"], w["conv_w"], w["w_target"],
                         chunk=c["chunk"], eta=c["eta"], max_tokens=c["T"])
         x = h0.to(torch.bfloat16)
         o = torch.empty_like(x)
-        sec, clk = timed(lambda: single.forward(x, doc_starts=(0,), out=o), steps, args.warmup)
+
+        def layer_calls():
+            for _ in range(c["n_layers"]):
+                single.forward(x, doc_starts=(0,), out=o)
+        sec, clk = timed(layer_calls, max(3, min(steps, 5)), 1)
         single.check()
-        emit("single TTT layer of the stack's shape", c["T"], sec, clk,
+        emit(f"single TTT layer of the stack's shape, {c['n_layers']} calls per step "
+             f"(layer-tokens)", c["n_layers"] * c["T"], sec, clk,
              {"workload": "stack-single-layer", "d": c["d"], "f": c["f"], "T": c["T"],
-              "chunk": c["chunk"]})
+              "chunk": c["chunk"], "calls_per_step": c["n_layers"]})
     return 0
 
 
