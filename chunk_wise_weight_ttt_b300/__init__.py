@@ -7,7 +7,7 @@ from ._abi import TTTError, TTT_BF16, TTT_F32  # noqa: F401
 
 
 def __getattr__(name):
-    if name in ("TTTMLP", "TTTStack", "rmsnorm", "residual_add", "workspace_bytes"):
+    if name in ("TTTMLP", "TTTStack", "rmsnorm", "residual_add", "residual_rmsnorm", "workspace_bytes"):
         from . import layer
         return getattr(layer, name)
     raise AttributeError(name)

@@ -57,6 +57,7 @@ SIGNATURES = {
                                  C.c_float, _vp, _vp, _vp]),
     "ttt_rmsnorm": (_st, [_vp, _vp, _i64, _i32, C.c_float, _i32, _vp]),
     "ttt_residual_add": (_st, [_vp, _vp, _i64, _i32, _i32, _vp]),
+    "ttt_residual_rmsnorm": (_st, [_vp, _vp, _vp, _i64, _i32, C.c_float, _i32, _i32, _vp]),
 }
 
 _lib = None

@@ -431,6 +431,36 @@ __global__ void rmsnorm_kernel(const float* __restrict__ h, TOut* __restrict__ x
   for (int i = threadIdx.x; i < d; i += blockDim.x) xr[i] = from_f<TOut>(hr[i] * inv);
 }
 
+// h[t] += o[t], then x[t] = RMSNorm(h[t]) (the next block's input), one block
+// per row: the residual add and the next RMSNorm of a pre-norm stack in one
+// pass over h.  The same arithmetic in the same order as residual_add_kernel
+// followed by rmsnorm_kernel with 256 threads, so the results are identical.
+template <typename TO, typename TX>
+__global__ void residual_rmsnorm_kernel(float* __restrict__ h, const TO* __restrict__ o,
+                                        TX* __restrict__ x, int d, float eps) {
+  float* hr = h + (long long)blockIdx.x * d;
+  const TO* orow = o + (long long)blockIdx.x * d;
+  float ss = 0.0f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float v = hr[i] + to_f(orow[i]);
+    hr[i] = v;
+    ss = fmaf(v, v, ss);
+  }
+  __shared__ float red[32];
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = (threadIdx.x < blockDim.x / 32) ? red[threadIdx.x] : 0.0f;
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float inv = rsqrtf(red[0] / (float)d + eps);
+  TX* xr = x + (long long)blockIdx.x * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) xr[i] = from_f<TX>(hr[i] * inv);
+}
+
 template <typename T>
 __global__ void residual_add_kernel(float* __restrict__ h, const T* __restrict__ o, long long n) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;

@@ -1235,6 +1235,28 @@ ttt_status ttt_residual_add(float* hs, const void* o, int64_t n, int32_t d, int3
   return TTT_OK;
 }
 
+ttt_status ttt_residual_rmsnorm(float* hs, const void* o, void* x, int64_t n, int32_t d, float eps,
+                                int32_t o_dtype, int32_t x_dtype, void* stream) {
+  if (n < 0 || d < 1 || (n > 0 && (!hs || !o || !x)) || (o_dtype != TTT_F32 && o_dtype != TTT_BF16) ||
+      (x_dtype != TTT_F32 && x_dtype != TTT_BF16))
+    return fail(nullptr, TTT_EINVAL, "ttt_residual_rmsnorm: bad arguments");
+  if (n == 0) return TTT_OK;
+  if (n > (int64_t(1) << 31) - 1) return fail(nullptr, TTT_EUNSUPPORTED, "ttt_residual_rmsnorm: too many rows");
+  cudaStream_t st = (cudaStream_t)stream;
+  const unsigned rows = (unsigned)n;
+  if (o_dtype == TTT_BF16 && x_dtype == TTT_BF16)
+    residual_rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<rows, 256, 0, st>>>(
+        hs, (const __nv_bfloat16*)o, (__nv_bfloat16*)x, d, eps);
+  else if (o_dtype == TTT_BF16)
+    residual_rmsnorm_kernel<__nv_bfloat16, float><<<rows, 256, 0, st>>>(hs, (const __nv_bfloat16*)o, (float*)x, d, eps);
+  else if (x_dtype == TTT_BF16)
+    residual_rmsnorm_kernel<float, __nv_bfloat16><<<rows, 256, 0, st>>>(hs, (const float*)o, (__nv_bfloat16*)x, d, eps);
+  else
+    residual_rmsnorm_kernel<float, float><<<rows, 256, 0, st>>>(hs, (const float*)o, (float*)x, d, eps);
+  TTT_CK(nullptr, cudaGetLastError());
+  return TTT_OK;
+}
+
 }  // extern "C"
 
 // ====================================================================== allocation-free target

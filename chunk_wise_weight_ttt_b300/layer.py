@@ -263,13 +263,16 @@ class TTTStack:
         x = torch.empty(h0.shape, dtype=self.dtype, device=h0.device)
         o = torch.empty_like(x)
         n = n_layers or len(self.blocks)
+        rmsnorm(h, x, self.eps, stream=stream)
         for li, blk in enumerate(self.blocks[:n]):
-            rmsnorm(h, x, self.eps, stream=stream)
             if is_ttt_layer(li, self.ttt_every):
                 blk.forward(x, x0, doc_starts=doc_starts, out=o, stream=stream)
             else:
                 blk.forward_static(x, out=o, stream=stream)
-            residual_add(h, o, stream=stream)
+            if li + 1 < n:
+                residual_rmsnorm(h, o, x, self.eps, stream=stream)  # and the next block's input
+            else:
+                residual_add(h, o, stream=stream)
         return h
 
     __call__ = forward
@@ -288,6 +291,16 @@ def rmsnorm(h: torch.Tensor, out: torch.Tensor, eps: float = 1e-6, stream=None) 
     lib = _abi.load()
     st = lib.ttt_rmsnorm(_ptr(h), _ptr(out), h.shape[0], h.shape[1], eps, _DT[out.dtype],
                          _stream(stream))
+    _check(lib, None, st)
+    return out
+
+
+def residual_rmsnorm(h: torch.Tensor, o: torch.Tensor, out: torch.Tensor, eps: float = 1e-6,
+                     stream=None) -> torch.Tensor:
+    """h += o, then out = RMSNorm(h), in one pass over h."""
+    lib = _abi.load()
+    st = lib.ttt_residual_rmsnorm(_ptr(h), _ptr(o), _ptr(out), h.shape[0], h.shape[1], eps,
+                                  _DT[o.dtype], _DT[out.dtype], _stream(stream))
     _check(lib, None, st)
     return out
 

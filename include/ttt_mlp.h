@@ -285,6 +285,12 @@ ttt_status ttt_rmsnorm(const float* h, void* x, int64_t n, int32_t d, float eps,
 ttt_status ttt_residual_add(float* h, const void* o, int64_t n, int32_t d, int32_t o_dtype,
                             void* stream);
 
+/* The two in one pass over h: h += o, then x = RMSNorm(h) (the next block's
+ * input).  The same results as ttt_residual_add followed by ttt_rmsnorm.
+ * h: n x d fp32; o: n x d of o_dtype; x: n x d of x_dtype. */
+ttt_status ttt_residual_rmsnorm(float* h, const void* o, void* x, int64_t n, int32_t d, float eps,
+                                int32_t o_dtype, int32_t x_dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -596,3 +596,24 @@ def test_rmsnorm_and_residual_glue():
     o = torch.from_numpy(rng.standard_normal((37, 256)).astype(np.float32)).cuda()
     residual_add(ht, o)
     assert np.allclose(_host(ht), np.float64(h) + _host(o), rtol=1e-6, atol=1e-6)
+
+
+@pytest.mark.parametrize("d,o_dt,x_dt", [(2560, torch.bfloat16, torch.bfloat16), (300, torch.float32, torch.float32),
+                                         (256, torch.bfloat16, torch.float32)])
+def test_residual_rmsnorm_equals_the_two_glue_calls(d, o_dt, x_dt):
+    """The fused residual add + next RMSNorm gives the same bits as the two
+    calls one after the other, and RMSNorm of h + o against the oracle."""
+    from chunk_wise_weight_ttt_b300 import residual_add, residual_rmsnorm, rmsnorm
+    rng = np.random.default_rng(d)
+    h = torch.from_numpy(rng.standard_normal((53, d)).astype(np.float32) * 2).cuda()
+    o = torch.from_numpy(rng.standard_normal((53, d)).astype(np.float32)).cuda().to(o_dt)
+    h1, h2 = h.clone(), h.clone()
+    x1 = torch.empty((53, d), dtype=x_dt, device="cuda")
+    x2 = torch.empty_like(x1)
+    residual_rmsnorm(h1, o, x1, 1e-6)
+    residual_add(h2, o)
+    rmsnorm(h2, x2, 1e-6)
+    torch.cuda.synchronize()
+    assert torch.equal(h1, h2) and torch.equal(x1, x2)
+    ref = orc.rms_norm(_host(h) + _host(o), 1e-6)
+    assert _rel(_host(x1), ref) < (4e-3 if x_dt == torch.bfloat16 else 1e-6)
