@@ -803,26 +803,29 @@ ttt_status forward_impl(ttt_mlp* h, int doc, const void* x, const void* x0, int6
 int64_t host_segment_tokens() {
   static const int64_t n = [] {
     const char* v = std::getenv("TTT_HOST_SEGMENT");
-    const long long t = v ? std::atoll(v) : 4096;
-    return (int64_t)(t >= 256 ? t : 4096);
+    const long long t = v ? std::atoll(v) : 8192;
+    return (int64_t)(t >= 256 ? t : 8192);
   }();
   return n;
 }
 
 // Where a host-buffer call is cut into segments: at group starts (chunk
-// starts on the fp32 path), the first segment at least half of
-// host_segment_tokens() long and the others at least host_segment_tokens()
-// (the first segment's input copy cannot overlap a layer, so it is kept
-// short).  A segment that starts at a group start and runs as a call of its
-// own makes the same chunks and groups, and so the same bits, as the whole
-// call: a group start is a chunk start, the conv window never crosses a
-// chunk, and the slot's state carries over.
+// starts on the fp32 path), every segment at least host_segment_tokens() long
+// except the last, which is the call's last group alone (its output copy is
+// the one no layer overlaps, so it is kept short).  On a handle with a shared
+// scratch the first segment is half as long as the others (its input copy
+// cannot overlap the previous call there).  A segment that starts at a group
+// start and runs as a call of its own makes the same chunks and groups, and so
+// the same bits, as the whole call: a group start is a chunk start, the conv
+// window never crosses a chunk, and the slot's state carries over.
 std::vector<int64_t> host_cuts(ttt_mlp* h, int64_t n, const int64_t* ds, int nds) {
   const std::vector<Span> groups = plan_groups(n, h->cfg.chunk, h->tc ? h->G : 1, ds, nds);
+  const int64_t seg = host_segment_tokens();
+  const int64_t first = h->owns_scratch ? seg : seg / 2;
   std::vector<int64_t> cuts{0};
   for (const Span& g : groups)
-    if (g.start - cuts.back() >= (cuts.size() == 1 ? host_segment_tokens() / 2 : host_segment_tokens()))
-      cuts.push_back(g.start);
+    if (g.start - cuts.back() >= (cuts.size() == 1 ? first : seg)) cuts.push_back(g.start);
+  if (groups.size() > 1 && groups.back().start > cuts.back()) cuts.push_back(groups.back().start);
   cuts.push_back(n);
   return cuts;
 }

@@ -165,8 +165,10 @@ ttt_status ttt_mlp_forward_static(ttt_mlp* h, const void* x, int64_t n_tokens, v
 
 /* The same call with host buffers: x_host / x0_host are copied to device
  * staging inside the workspace, the layer runs, and O is copied back into
- * o_host.  The call is cut at group starts into segments of about 4096 tokens
- * (TTT_HOST_SEGMENT overrides), which give the same bits as one call; segment
+ * o_host.  The call is cut at group starts into segments of about 8192 tokens
+ * (TTT_HOST_SEGMENT overrides), the last segment being the call's last group
+ * alone (its output copy is the one no layer overlaps); the segments give the
+ * same bits as one call; segment
  * k+1's input copy and segment k-1's output copy run on two copy streams of
  * the handle while segment k runs on `stream`.  The output copies start after
  * everything already enqueued on `stream`, and `stream` waits for the last

@@ -469,10 +469,11 @@ def test_host_buffer_entry_point():
 
 
 def test_host_buffer_segments_equal_device_call():
-    """A host-buffer call cut into five segments (at 2048, a document start,
-    and at 6144, 11048 and 15144, group starts inside documents), with an X0
-    that differs from X, equals the device-buffer call bit for bit, output and
-    final state."""
+    """A host-buffer call cut into five segments at group starts (4096, 8192,
+    13096 and 19049, the last segment being the call's last group alone; the
+    call has documents starting at 2048, 9000 and 17001, off the cuts), with
+    an X0 that differs from X, equals the device-buffer call bit for bit,
+    output and final state."""
     cfg = make_layer(256, 512, 20000, 64, 4, 0.5, dtype="bf16", seed=5, init="qwen",
                      doc_starts=(0, 2048, 9000, 17001))
     dt = torch.bfloat16
