@@ -125,8 +125,15 @@ def group_tokens() -> int:
 
 
 def kernel_hash() -> str:
-    with open(KERNEL_SRC, "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()[:16]
+    """sha256 prefix of the kernel source's code: comments and blank space
+    are dropped first, so that a comment edit keeps the stored counters."""
+    import re
+    with open(KERNEL_SRC) as fh:
+        src = fh.read()
+    src = re.sub(r"//[^\n]*", "", src)
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    code = "\n".join(line.strip() for line in src.splitlines() if line.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 def stored_traffic(groups_per_launch: float, chunk: int, d: int, f: int):

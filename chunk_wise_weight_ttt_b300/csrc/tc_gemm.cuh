@@ -856,7 +856,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       epilogue_tile<MODE>(a, ti, tacc, row, staging + (warp - 2) * kStgBytesPerWarp);
       if (MODE == kGroup) {
         if (ti.kind == 1) {
-          // W and the bf16 copy are stored: make them visible to the next
+          // the new hi and lo planes are stored: make them visible to the next
           // group's TMA (async-proxy) reads and ordinary reads on other SMs
           fence_proxy_async_global();
           __threadfence();
