@@ -1,6 +1,7 @@
 // Inline-PTX building blocks for sm_100-family (sm_103a) kernels: mbarriers
 // (local and across a CTA pair of a cluster), TMA tensor loads into one CTA's
-// own shared memory (no multicast loads) and L2 prefetches, and the
+// own shared memory (no multicast loads), TMA tensor stores from it, L2
+// prefetches, and the
 // 5th-generation tensor core in its CTA-pair form (tcgen05 cta_group::2: TMEM
 // allocation, MMA issue, commit, TMEM loads).  Every mbarrier wait here is
 // bounded by wall-clock time so that no kernel can hang the GPU.
@@ -24,6 +25,7 @@ enum : int {
   kErrWaitSched = 5,
   kErrWaitDrain = 6,
   kErrWaitDep = 7,
+  kErrWaitEpi = 8,
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -199,6 +201,40 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32
                    reinterpret_cast<uint64_t>(map)),
                "r"(c0), "r"(c1)
                : "memory");
+}
+
+// Store of one box from this CTA's shared memory (laid out as a load through
+// the same map would lay it out) to global memory, as part of the issuing
+// thread's current bulk group.  Elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int32_t c0,
+                                             int32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+// Close the issuing thread's current bulk group of TMA stores.
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Block until at most N of this thread's committed bulk groups are still
+// reading their shared-memory sources (their buffers may then be rewritten).
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Block until at most N of this thread's committed bulk groups are incomplete
+// (the others' global writes are done).
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05

@@ -6,9 +6,8 @@
 // in its shared memory, the even CTA issues the MMAs for both, and each CTA's
 // TMEM receives its 128 accumulator rows.  A ring stage is therefore 32 KB per
 // CTA and carries 1.5x the MMA work per byte of a 128x256 tile.  The group
-// kernel has 6 stages plus the update tiles' transpose staging; the other
-// modes need no staging and use its space for a seventh stage (the operand
-// stream is latency-bound, so the deeper ring keeps more bytes in flight).
+// kernel has 5 stages plus two state-slice buffers per epilogue warp for its
+// update tiles (a sixth stage measured no faster); the other modes have 7.
 // The even CTA (the leader) claims tiles from a dynamic counter and hands each
 // to its peer through distributed shared memory; both CTAs' TMA loads signal
 // the leader's ring barriers, and the leader's commits release the stages and
@@ -48,12 +47,14 @@
 //            and lo, the signed remainder, so (hi << 16) + lo is W's bits
 //            exactly.  hi is double-buffered (the apply tiles of a group read
 //            the plane that its update tiles do not write).  An update tile
-//            accumulates V_g^T Z_g from zero in TMEM; its epilogue rebuilds
-//            the fp32 block of W_s from hi and lo (or, at a document start,
-//            takes W_0), adds in one fp32 rounding (read in a coalesced
-//            layout, one 64-column slice ahead, after the producer prefetched
-//            both planes into L2 at the tile's start) and stores the new
-//            planes, coalesced through a per-warp shared-memory transpose.
+//            accumulates V_g^T Z_g from zero in TMEM.  Its epilogue works in
+//            64-column slices of each warp's 32 rows: TMA brings the slice's
+//            block of both planes (or, at a document start, of W_0) into
+//            shared memory (two slices in flight; the producer prefetched the
+//            tile's block into L2 when the tile started), each thread rebuilds
+//            its row's fp32 W_s there, adds the accumulator row from TMEM in
+//            one fp32 rounding, writes the new planes back in place, and TMA
+//            stores them.  No state byte passes through the load/store units.
 //            Against a separate fp32 state and bf16 copy this writes 4 bytes
 //            of state per element and group instead of 6, and the apply and
 //            update tiles read the same hi plane.
@@ -97,9 +98,12 @@ constexpr int kMaxGroups = 256;
 // 24 and 48 pairs, 32 gave the fastest step.
 constexpr int kSwizzlePairs = 32;
 constexpr uint16_t kPairMask = 0x3;  // both CTAs of the cluster
-// per-warp staging for the transposed (coalesced) update-tile stores: 32 rows
-// of a 64-column fp32 slice
-constexpr int kStgBytesPerWarp = 32 * 256;
+// Update-tile epilogue buffers, per epilogue warp: two slice buffers, each the
+// hi and the lo plane of a 32-row x 64-column block of W as TMA lays out a box
+// with 128-byte swizzle (16-byte chunk q of row r at q ^ (r % 8)).
+constexpr int kEpiBoxBytes = 32 * 128;              // one plane of one slice
+constexpr int kEpiBufBytes = 2 * kEpiBoxBytes;      // hi, then lo
+constexpr int kEpiBytesPerWarp = 2 * kEpiBufBytes;  // two slices in flight
 constexpr int kEpiWarps = 4;
 
 enum GemmMode : int { kSwiGLU = 0, kLinear = 1, kSGram = 2, kGroup = 3, kDGram = 4 };
@@ -113,8 +117,9 @@ enum GemmMode : int { kSwiGLU = 0, kLinear = 1, kSGram = 2, kGroup = 3, kDGram =
 //            3 V MN-major (64x64), 4 V MN-major with the run's K extent,
 //            5 Z MN-major (64x64) with the run's K extent,
 //            6 lo of the slot (64x128, L2-prefetch boxes), 7 hi[1] (64x128),
-//            8 W_0 bf16 (64x128)
-constexpr int kNumMaps = 9;
+//            8 W_0 bf16 (64x128); the update epilogue's 64x32 boxes:
+//            9 hi[0], 10 hi[1], 11 lo, 12 W_0
+constexpr int kNumMaps = 13;
 
 // kGroup per-group flags
 constexpr uint8_t kGrpReset = 1;  // document start: the group's state is W_0
@@ -131,9 +136,6 @@ struct GemmArgs {
   int* counter;  // dynamic tile-pair counter, zero at launch
   int* err;      // workspace error word
   void* out0;    // kSwiGLU: Z; kLinear: V or O (n_rows x d); kSGram: S; kGroup: O
-  void* lo;      // kGroup: the lo plane of the slot's state (updated in place)
-  void* hi[2];   // kGroup: the slot's two hi planes (read / written alternately)
-  const void* w0;  // kGroup: W_0 (bf16)
   // groups
   int s_pad;         // row/column pitch of one S block (multiple of 256)
   int n_groups;      // groups of the launch (kSGram, kDGram, kGroup)
@@ -336,15 +338,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // rounded to bf16).
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-// 16-byte global load cached in L2 only.
-__device__ __forceinline__ uint4 ld_cg_u4(const uint16_t* p) {
-  uint4 v;
-  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // The two 16-bit planes of an fp32 value's bits b: hi = the upper half
 // rounded half up in magnitude (a bf16 within half an ulp of the value; b +
 // 0x8000 cannot carry into the sign for a finite value), lo = b - (hi << 16)
@@ -384,7 +377,7 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t
 
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo& ti,
-                                              uint32_t tacc, int row, uint8_t* stg) {
+                                              uint32_t tacc, int row) {
   uint32_t r[32];
   if (MODE == kSwiGLU) {
     const int grow = ti.m0 + row;
@@ -407,120 +400,23 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
       if (grow < a.n_rows) store_bf16x32(zrow + col, p, a.f - col);
     }
   } else if (MODE == kLinear || MODE == kGroup) {
-    if (MODE == kGroup && ti.kind == 1) {
-      // fast-weight update: W <- W_s + acc (acc = V^T Z of the group, from
-      // zero), one fp32 rounding.  The warp's 32 rows go in four 64-column
-      // slices: TMEM -> registers (row per thread, 32 columns per load) ->
-      // staging (256-byte rows of 16-byte chunks, chunk q of row r at
-      // q ^ (r % 8): both phases bank-conflict free) -> the coalesced layout,
-      // where a thread owns 8 consecutive columns of a row, so that 8 lanes
-      // cover a row's 128 bytes of a plane and every global access of the warp
-      // is 4 whole lines.  There the thread rebuilds W_s from its hi and lo
-      // planes (read one slice ahead), adds, and stores the new planes.
-      const int lane = row & 31;
-      const int rbase = ti.m0 + (row - lane);
-      const uint8_t fl = a.g_flags[ti.g];
-      const bool from_w0 = fl & kGrpReset;
-      const uint16_t* HI = reinterpret_cast<const uint16_t*>(a.hi[(fl & kGrpInWb1) ? 1 : 0]);
-      uint16_t* HO = reinterpret_cast<uint16_t*>(a.hi[(fl & kGrpOutWb1) ? 1 : 0]);
-      uint16_t* LO = reinterpret_cast<uint16_t*>(a.lo);
-      const uint16_t* W0 = reinterpret_cast<const uint16_t*>(a.w0);
-      const uint32_t stg_u = smem_u32(stg);
-      const uint32_t st_row = stg_u + lane * 256;
-      const int cq = lane & 7;
-      uint4 hc[8], lc[8], hn[8], ln[8];  // W_s planes, 8 columns per entry (rows 4j + lane / 8)
-      auto load_w = [&](int u, uint4 (&hd)[8], uint4 (&ld)[8]) {
-        const int col = ti.n0 + u * 64 + cq * 8;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int wr = rbase + j * 4 + (lane >> 3);
-          hd[j] = make_uint4(0u, 0u, 0u, 0u);
-          ld[j] = make_uint4(0u, 0u, 0u, 0u);
-          if (wr < a.d && col < a.f) {
-            const size_t off = (size_t)wr * a.f + col;
-            if (from_w0) {
-              hd[j] = ld_cg_u4(W0 + off);
-            } else {
-              hd[j] = ld_cg_u4(HI + off);
-              ld[j] = ld_cg_u4(LO + off);
-            }
-          }
-        }
-      };
-      load_w(0, hc, lc);
-#pragma unroll
-      for (int u = 0; u < kBN / 64; ++u) {
-        if (u + 1 < kBN / 64) load_w(u + 1, hn, ln);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          tmem_ld32(tacc + u * 64 + half * 32, r);
-          tmem_ld_wait(r);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            st_shared_v4(st_row + (((half * 8 + q) ^ (lane & 7)) << 4), r[4 * q], r[4 * q + 1],
-                         r[4 * q + 2], r[4 * q + 3]);
-        }
-        __syncwarp();
-        const int col = ti.n0 + u * 64 + cq * 8;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int rr = j * 4 + (lane >> 3);
-          uint32_t v[8];
-          {
-            uint32_t t0[4], t1[4];
-            ld_shared_v4(stg_u + rr * 256 + (((2 * cq) ^ (rr & 7)) << 4), t0);
-            ld_shared_v4(stg_u + rr * 256 + (((2 * cq + 1) ^ (rr & 7)) << 4), t1);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              v[e] = t0[e];
-              v[4 + e] = t1[e];
-            }
-          }
-          const int wr = rbase + rr;
-          if (wr < a.d && col < a.f) {
-            const uint32_t hw[4] = {hc[j].x, hc[j].y, hc[j].z, hc[j].w};
-            const uint32_t lw[4] = {lc[j].x, lc[j].y, lc[j].z, lc[j].w};
-            uint32_t ho[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t b0 = __float_as_uint(__uint_as_float(join_hi_lo(hw[e], lw[e])) +
-                                                  __uint_as_float(v[2 * e]));
-              const uint32_t b1 = __float_as_uint(__uint_as_float(join_hi_lo(hw[e] >> 16, lw[e] >> 16)) +
-                                                  __uint_as_float(v[2 * e + 1]));
-              const uint32_t h0 = hi_of(b0), h1 = hi_of(b1);
-              ho[e] = h0 | (h1 << 16);
-              lo[e] = lo_of(b0, h0) | (lo_of(b1, h1) << 16);
-            }
-            const size_t off = (size_t)wr * a.f + col;
-            *reinterpret_cast<uint4*>(HO + off) = make_uint4(ho[0], ho[1], ho[2], ho[3]);
-            *reinterpret_cast<uint4*>(LO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          }
-        }
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          hc[j] = hn[j];
-          lc[j] = ln[j];
-        }
-      }
-    } else {
-      // plain bf16 store of alpha * acc (kLinear) or acc (kGroup apply)
-      const float alpha = (MODE == kLinear) ? a.alpha : 1.0f;
-      const int grow = (MODE == kLinear) ? ti.m0 + row : a.g_start[ti.g] + ti.m0 + row;
-      const bool ok = (MODE == kLinear) ? (grow < a.n_rows) : (ti.m0 + row < a.g_len[ti.g]);
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out0) + (size_t)grow * a.d;
+    // plain bf16 store of alpha * acc (kLinear) or acc (the apply tiles of
+    // kGroup; its update tiles have their own epilogue, update_epilogue)
+    const float alpha = (MODE == kLinear) ? a.alpha : 1.0f;
+    const int grow = (MODE == kLinear) ? ti.m0 + row : a.g_start[ti.g] + ti.m0 + row;
+    const bool ok = (MODE == kLinear) ? (grow < a.n_rows) : (ti.m0 + row < a.g_len[ti.g]);
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out0) + (size_t)grow * a.d;
 #pragma unroll 1
-      for (int s = 0; s < kBN / 32; ++s) {
-        tmem_ld32(tacc + s * 32, r);
-        tmem_ld_wait(r);
-        uint32_t p[16];
+    for (int s = 0; s < kBN / 32; ++s) {
+      tmem_ld32(tacc + s * 32, r);
+      tmem_ld_wait(r);
+      uint32_t p[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          p[j] = pack_bf16x2(alpha * __uint_as_float(r[2 * j]),
-                             alpha * __uint_as_float(r[2 * j + 1]));
-        const int col = ti.n0 + s * 32;
-        if (ok) store_bf16x32(orow + col, p, a.d - col);
-      }
+      for (int j = 0; j < 16; ++j)
+        p[j] = pack_bf16x2(alpha * __uint_as_float(r[2 * j]),
+                           alpha * __uint_as_float(r[2 * j + 1]));
+      const int col = ti.n0 + s * 32;
+      if (ok) store_bf16x32(orow + col, p, a.d - col);
     }
   } else if (MODE == kDGram) {
     // same-chunk entries of the Gram block in fp32, everything else 0
@@ -574,15 +470,130 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const TileInfo&
   }
 }
 
+// The update tiles' epilogue state of one epilogue warp: its two slice
+// buffers (`buf`, kEpiBytesPerWarp bytes, 1024-byte aligned), their TMA
+// barriers, the barriers' phase bits and which buffers have a load in flight.
+struct SliceBuffers {
+  uint8_t* buf;
+  uint64_t* bar;  // [2]
+  uint32_t phase;
+  uint32_t pending;
+};
+
+// The maps the update epilogue of group g reads its state from and writes it to.
+__device__ __forceinline__ const CUtensorMap* upd_hi_in(const GemmArgs& a, int g) {
+  const uint8_t fl = a.g_flags[g];
+  return (fl & kGrpReset) ? &a.map[12] : (fl & kGrpInWb1) ? &a.map[10] : &a.map[9];
+}
+__device__ __forceinline__ const CUtensorMap* upd_hi_out(const GemmArgs& a, int g) {
+  return (a.g_flags[g] & kGrpOutWb1) ? &a.map[10] : &a.map[9];
+}
+
+// Whether slice u of this warp's rows holds any element of W (d x f): a
+// slice wholly outside (a tile past a d or f that is not a multiple of 256)
+// is neither loaded nor stored.
+__device__ __forceinline__ bool upd_slice_live(const GemmArgs& a, const TileInfo& ti, int sub, int u) {
+  return ti.m0 + sub * 32 < a.d && ti.n0 + u * 64 < a.f;
+}
+
+// Lane 0: start the TMA loads of slice u (64 columns) of this warp's 32 rows of
+// W_s into buffer b: the hi plane (W_0's bf16 values at a document start) and
+// the lo plane (none at a document start: it is zero there).  A dead slice
+// completes the barrier's phase with no bytes.
+__device__ __forceinline__ void upd_load_slice(const GemmArgs& a, const TileInfo& ti, int sub, int u,
+                                               int b, SliceBuffers& sb) {
+  const bool from_w0 = a.g_flags[ti.g] & kGrpReset;
+  const bool live = upd_slice_live(a, ti, sub, u);
+  uint8_t* dst = sb.buf + b * kEpiBufBytes;
+  const uint32_t bar = smem_u32(&sb.bar[b]);
+  const int c0 = ti.n0 + u * 64, r0 = ti.m0 + sub * 32;
+  mbar_arrive_expect_tx(&sb.bar[b], !live ? 0 : from_w0 ? kEpiBoxBytes : kEpiBufBytes);
+  if (!live) return;
+  tma_load_2d_pair(dst, upd_hi_in(a, ti.g), bar, c0, r0);
+  if (!from_w0) tma_load_2d_pair(dst + kEpiBoxBytes, &a.map[11], bar, c0, r0);
+}
+
+// Fast-weight update of one update tile, for one epilogue warp (its 32 rows,
+// one per lane): W <- W_s + acc in one fp32 rounding, in four 64-column
+// slices.  The loads of slices 0 and 1 were started before the accumulator
+// was ready (upd_load_slice).  Per slice: wait for its state block, take the
+// accumulator row from TMEM, rebuild W_s from the planes in shared memory,
+// add, write the new planes over the old ones, and TMA-store them (the hi
+// plane to the group's output plane, lo in place); the buffer then takes
+// slice u + 2.  The global writes complete in the caller (bulk_wait_group).
+// Returns false if a wait ran out.
+__device__ __forceinline__ bool update_epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t tacc,
+                                                int sub, int lane, SliceBuffers& sb,
+                                                volatile int* abort_flag) {
+  const bool from_w0 = a.g_flags[ti.g] & kGrpReset;
+  const CUtensorMap* m_out = upd_hi_out(a, ti.g);
+  const int r0 = ti.m0 + sub * 32;
+  uint32_t r[32], v[32];
+#pragma unroll 1
+  for (int u = 0; u < kBN / 64; ++u) {
+    const int b = u & 1;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(&sb.bar[b], (sb.phase >> b) & 1u, abort_flag, a.err, kErrWaitEpi);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) return false;
+    sb.phase ^= 1u << b;
+    sb.pending &= ~(1u << b);
+    tmem_ld32(tacc + u * 64, r);
+    tmem_ld_wait(r);
+    tmem_ld32(tacc + u * 64 + 32, v);
+    tmem_ld_wait(v);
+    // this lane's row of the slice: 8 chunks of 8 columns per plane
+    const uint32_t hrow = smem_u32(sb.buf + b * kEpiBufBytes) + lane * 128;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t off = static_cast<uint32_t>((q ^ (lane & 7)) << 4);
+      uint32_t hw[4], lw[4] = {0u, 0u, 0u, 0u};
+      ld_shared_v4(hrow + off, hw);
+      if (!from_w0) ld_shared_v4(hrow + kEpiBoxBytes + off, lw);
+      uint32_t ho[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t d0 = q < 4 ? r[8 * q + 2 * e] : v[8 * (q - 4) + 2 * e];
+        const uint32_t d1 = q < 4 ? r[8 * q + 2 * e + 1] : v[8 * (q - 4) + 2 * e + 1];
+        const uint32_t b0 = __float_as_uint(__uint_as_float(join_hi_lo(hw[e], lw[e])) + __uint_as_float(d0));
+        const uint32_t b1 =
+            __float_as_uint(__uint_as_float(join_hi_lo(hw[e] >> 16, lw[e] >> 16)) + __uint_as_float(d1));
+        const uint32_t h0 = hi_of(b0), h1 = hi_of(b1);
+        ho[e] = h0 | (h1 << 16);
+        lo[e] = lo_of(b0, h0) | (lo_of(b1, h1) << 16);
+      }
+      st_shared_v4(hrow + off, ho[0], ho[1], ho[2], ho[3]);
+      st_shared_v4(hrow + kEpiBoxBytes + off, lo[0], lo[1], lo[2], lo[3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      uint8_t* src = sb.buf + b * kEpiBufBytes;
+      if (upd_slice_live(a, ti, sub, u)) {
+        tma_store_2d(m_out, src, ti.n0 + u * 64, r0);
+        tma_store_2d(&a.map[11], src + kEpiBoxBytes, ti.n0 + u * 64, r0);
+      }
+      bulk_commit_group();
+      if (u + 2 < kBN / 64) {
+        bulk_wait_group_read<0>();  // the stores have read the buffer
+        upd_load_slice(a, ti, sub, u + 2, b, sb);
+      }
+    }
+    if (u + 2 < kBN / 64) sb.pending |= 1u << b;
+    __syncwarp();
+  }
+  return true;
+}
+
 // Ring depth and dynamic shared memory of each mode.
 template <int MODE>
 __host__ __device__ constexpr int stages_of() {
-  return MODE == kGroup ? 6 : 7;
+  return MODE == kGroup ? 5 : 7;
 }
 template <int MODE>
 __host__ __device__ constexpr int smem_bytes_of() {
   return 1024 /*align*/ + stages_of<MODE>() * kStageBytes + 1024 /*barriers*/ +
-         (MODE == kGroup ? kEpiWarps * kStgBytesPerWarp : 0);
+         (MODE == kGroup ? kEpiWarps * kEpiBytesPerWarp : 0);
 }
 
 template <int MODE>
@@ -602,10 +613,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   uint64_t* sched_full = acc_empty + 2;        // [kSchedRing]
   uint64_t* sched_empty = sched_full + kSchedRing;  // [kSchedRing] (used in the leader)
   uint64_t* drain = sched_empty + kSchedRing;  // [1]
-  int* sched_item = reinterpret_cast<int*>(drain + 1);  // [kSchedRing]
+  uint64_t* epi_bar = drain + 1;               // [kEpiWarps][2] (update-tile state loads)
+  int* sched_item = reinterpret_cast<int*>(epi_bar + 2 * kEpiWarps);  // [kSchedRing]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sched_item + kSchedRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  uint8_t* staging = smem + kStages * kStageBytes + 1024;  // [kEpiWarps][kStgBytesPerWarp]
+  // [kEpiWarps][kEpiBytesPerWarp], 1024-byte aligned (128-byte swizzle boxes)
+  uint8_t* epi_smem = smem + kStages * kStageBytes + 1024;
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -636,6 +649,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       mbar_init(&sched_empty[s], 2 + 2 * kEpiWarps);
     }
     mbar_init(drain, 1);
+    for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(&epi_bar[b], 1);  // the loading lane's expect
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -819,6 +833,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     // ---------------- epilogue warps
     const int sub = warp & 3;  // TMEM sub-partition this warp may access
     const int row = sub * 32 + lane;
+    SliceBuffers sb{epi_smem + (warp - 2) * kEpiBytesPerWarp, epi_bar + (warp - 2) * 2, 0u, 0u};
     int acc_it = 0;
 #pragma unroll 1
     for (int it = 0;; ++it) {
@@ -836,6 +851,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       if (t >= ntiles) break;
       const TileInfo ti = decode_tile<MODE>(a, t, rank);
       if (!ti.valid) continue;
+      const bool upd = MODE == kGroup && ti.kind == 1;
+      if (upd) {
+        if (ti.g > 0) {
+          // this tile rewrites the lo block that the previous group's update
+          // tile wrote and the hi rows that its apply tiles read
+          const int blk = ti.m0 / kBN;
+          int okd = 1;
+          if (lane == 0) {
+            okd = dep_wait(upd_counter(a, ti.g - 1, blk), upd_target(a), abort_flag, a.err, kErrWaitDep);
+            if (okd)
+              okd = dep_wait(app_counter(a, ti.g - 1, blk), app_target(a, ti.g - 1), abort_flag, a.err,
+                             kErrWaitDep);
+            fence_proxy_async_global();  // their writes before our TMA reads
+          }
+          if (!__shfl_sync(0xffffffffu, okd, 0)) break;
+        }
+        // the state of the first two slices streams in while the MMAs finish
+        if (lane == 0) {
+          upd_load_slice(a, ti, sub, 0, 0, sb);
+          upd_load_slice(a, ti, sub, 1, 1, sb);
+        }
+        sb.pending = 3u;
+      }
       const int buf = acc_it & 1;
       if (lane == 0)
         ok = mbar_wait(&acc_full[buf], (acc_it >> 1) & 1, abort_flag, a.err, kErrWaitAccFull);
@@ -843,32 +881,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       if (!ok) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + buf * kBN;
-      if (MODE == kGroup && ti.kind == 1 && ti.g > 0) {
-        // this tile rewrites the W block and the bf16 rows that the previous
-        // group's update tiles wrote and its apply tiles read
-        const int blk = ti.m0 / kBN;
-        int okd = dep_wait(upd_counter(a, ti.g - 1, blk), upd_target(a), abort_flag, a.err, kErrWaitDep);
-        if (okd)
-          okd = dep_wait(app_counter(a, ti.g - 1, blk), app_target(a, ti.g - 1), abort_flag, a.err,
-                         kErrWaitDep);
-        if (!__all_sync(0xffffffffu, okd)) break;
-      }
-      epilogue_tile<MODE>(a, ti, tacc, row, staging + (warp - 2) * kStgBytesPerWarp);
-      if (MODE == kGroup) {
-        if (ti.kind == 1) {
-          // the new hi and lo planes are stored: make them visible to the next
-          // group's TMA (async-proxy) reads and ordinary reads on other SMs
+      if (upd) {
+        const bool okw = update_epilogue(a, ti, tacc, sub, lane, sb, abort_flag);
+        // the accumulator is read (or abandoned): hand it back first
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_leader(&acc_empty[buf]);
+        if (!okw) break;
+        if (lane == 0) {
+          // the new planes are in global memory before the next group's
+          // tiles are told (they read them through TMA)
+          bulk_wait_group<0>();
           fence_proxy_async_global();
           __threadfence();
+          dep_signal(upd_counter(a, ti.g, ti.m0 / kBN), 1);
         }
         __syncwarp();
-        if (lane == 0)
-          dep_signal(ti.kind == 1 ? upd_counter(a, ti.g, ti.m0 / kBN) : app_counter(a, ti.g, ti.n0 / kBN), 1);
+      } else {
+        epilogue_tile<MODE>(a, ti, tacc, row);
+        if (MODE == kGroup) {
+          __syncwarp();
+          if (lane == 0) dep_signal(app_counter(a, ti.g, ti.n0 / kBN), 1);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_leader(&acc_empty[buf]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_leader(&acc_empty[buf]);
       ++acc_it;
+    }
+    if (MODE == kGroup && lane == 0) {
+      // before the CTA's shared memory is released: state loads still in
+      // flight land, and the stores have read their buffers
+      volatile int never = 0;
+      for (int b2 = 0; b2 < 2; ++b2)
+        if (sb.pending & (1u << b2)) mbar_wait(&sb.bar[b2], (sb.phase >> b2) & 1u, &never, a.err, kErrWaitDrain);
+      bulk_wait_group<0>();
     }
   }
 

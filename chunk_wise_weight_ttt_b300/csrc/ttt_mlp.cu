@@ -494,10 +494,16 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
   const size_t wsz = (size_t)d * f;
   uint16_t* hi[2] = {h->Whi + (size_t)doc * 2 * wsz, h->Whi + (size_t)doc * 2 * wsz + wsz};
   uint16_t* lo = h->Wlo + (size_t)doc * wsz;
-  CUtensorMap map_hi[2], map_lo;  // the slot's state planes (operand / L2-prefetch boxes)
+  // the slot's state planes: operand and L2-prefetch boxes (64 x 128), and the
+  // update epilogue's boxes (64 x 32) of both planes and of W_0
+  CUtensorMap map_hi[2], map_lo, map_hi_e[2], map_lo_e, map_w0_e;
   if (!make_map(&map_hi[0], hi[0], f, d, f, 64, 128, &why) ||
       !make_map(&map_hi[1], hi[1], f, d, f, 64, 128, &why) ||
-      !make_map(&map_lo, lo, f, d, f, 64, 128, &why))
+      !make_map(&map_lo, lo, f, d, f, 64, 128, &why) ||
+      !make_map(&map_hi_e[0], hi[0], f, d, f, 64, 32, &why) ||
+      !make_map(&map_hi_e[1], hi[1], f, d, f, 64, 32, &why) ||
+      !make_map(&map_lo_e, lo, f, d, f, 64, 32, &why) ||
+      !make_map(&map_w0_e, h->w0, f, d, f, 64, 32, &why))
     return fail(h, TTT_ECUDA, why);
   for (size_t w0 = 0; w0 < groups.size(); w0 += (size_t)h->s_slots) {
     const size_t w1 = std::min(groups.size(), w0 + (size_t)h->s_slots);
@@ -577,6 +583,10 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
       q.map[6] = map_lo;
       q.map[7] = map_hi[1];
       q.map[8] = h->map_w0;
+      q.map[9] = map_hi_e[0];
+      q.map[10] = map_hi_e[1];
+      q.map[11] = map_lo_e;
+      q.map[12] = map_w0_e;
       if (exact(e)) {
         q.map[4] = map_vmn;
         q.map[5] = map_zmn;
@@ -609,10 +619,6 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
       q.g_tile[q.n_groups] = tiles;
       q.slot0 = (int)(i - w0);
       q.out0 = o;
-      q.lo = lo;
-      q.hi[0] = hi[0];
-      q.hi[1] = hi[1];
-      q.w0 = h->w0;
       int* ctr = next_counters(h, st, 1 + 2 * q.n_groups * npd);
       q.counter = ctr;
       q.dep = ctr + 1;
