@@ -622,7 +622,11 @@ ttt_status forward_tc(ttt_mlp* h, int doc, const void* x, const void* x0, int64_
       int* ctr = next_counters(h, st, 1 + 2 * q.n_groups * npd);
       q.counter = ctr;
       q.dep = ctr + 1;
+      // failure-path test hook: the first group launch of the call withholds
+      // one of its own operand loads (its bounded waits then run out)
+      q.test_withhold_block = (i == 0 && fault_injected("group_wait")) ? 1 : 0;
       TTT_CK(h, launch_gemm<kGroup>(h, q, tiles, st));
+      q.test_withhold_block = 0;
       h->prof_launches++;
       h->prof_group_launches++;
       h->hcur[doc] = (uint8_t)cur;

@@ -49,8 +49,11 @@
  *     target-projection kernel withhold one of its own operand loads, so
  *     that kernel's bounded waits run out (about 4 s): the call itself
  *     succeeds, ttt_mlp_check then reports TTT_ETIMEOUT, and the slot's fast
- *     weight is undefined until it is reset.  (Tests the failure path
- *     without faulting the GPU.)
+ *     weight is undefined until it is reset.  TTT_FAULT=group_wait does the
+ *     same in the call's first fused apply+update (group) launch, whose
+ *     other tiles then time out on the completion counters the withheld
+ *     tile never raises.  (Both test the failure path without faulting the
+ *     GPU.)
  */
 #ifndef TTT_MLP_H
 #define TTT_MLP_H

@@ -557,18 +557,22 @@ def test_fault_injection_leaves_handle_usable(monkeypatch):
     assert _rel(_host(o), o_ref) < TOL_BF16
 
 
-def test_bounded_wait_runs_out_and_handle_recovers(monkeypatch):
+@pytest.mark.parametrize("hook,T", [("kernel_wait", 512), ("group_wait", 4096)])
+def test_bounded_wait_runs_out_and_handle_recovers(monkeypatch, hook, T):
     """TTT_FAULT=kernel_wait makes the target-projection kernel withhold one of
-    its own operand loads: the barrier that waits for it never completes, the
-    kernel's bounded waits run out (no GPU fault, no hang), ttt_mlp_check
-    reports TTT_ETIMEOUT, and after a reset the handle computes correctly."""
+    its own operand loads, TTT_FAULT=group_wait the fused apply+update kernel
+    (a launch of two chained groups here, so tiles of the second group wait on
+    the withheld tile's completion counter too): the barrier that waits for
+    the load never completes, the kernel's bounded waits run out (no GPU
+    fault, no hang), ttt_mlp_check reports TTT_ETIMEOUT, and after a reset the
+    handle computes correctly."""
     import time
     from chunk_wise_weight_ttt_b300 import TTTError
-    cfg = _bf16_cfg(T=512, C=64)
+    cfg = _bf16_cfg(T=T, C=64)
     layer, dt = _make_gpu_layer(cfg)
     x = _dev(cfg["x"], dt)
     layer.check()
-    monkeypatch.setenv("TTT_FAULT", "kernel_wait")
+    monkeypatch.setenv("TTT_FAULT", hook)
     t0 = time.time()
     layer.forward(x)  # enqueued: the failure is asynchronous
     monkeypatch.delenv("TTT_FAULT")
