@@ -21,7 +21,9 @@
 //               leader, issues the pair's tcgen05.mma from one thread.
 //   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (one TMEM
 //               lane = one output row per thread), the mode's arithmetic, and
-//               global stores; the other accumulator is filled meanwhile.
+//               the stores (through TMA for the group kernel's fast-weight
+//               state, plain global stores otherwise); the other accumulator
+//               is filled meanwhile.
 //
 // Modes (what the tiles are):
 //   kSwiGLU  Z = SiLU(X Wg^T) (.) (X Wu^T): the B tile stacks 128 rows of Wg
