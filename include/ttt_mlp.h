@@ -169,9 +169,10 @@ ttt_status ttt_mlp_forward_static(ttt_mlp* h, const void* x, int64_t n_tokens, v
 /* The same call with host buffers: x_host / x0_host are copied to device
  * staging inside the workspace, the layer runs, and O is copied back into
  * o_host.  The call is cut at group starts into segments of about 8192 tokens
- * (TTT_HOST_SEGMENT overrides), the last segment being the call's last group
- * alone (its output copy is the one no layer overlaps); the segments give the
- * same bits as one call; segment
+ * (TTT_HOST_SEGMENT overrides; on a shared scratch the first segment is half
+ * as long, since its input copy cannot overlap the previous call there), the
+ * last segment being the call's last group alone (its output copy is the one
+ * no layer overlaps); the segments give the same bits as one call.  Segment
  * k+1's input copy and segment k-1's output copy run on two copy streams of
  * the handle while segment k runs on `stream`.  The output copies start after
  * everything already enqueued on `stream`, and `stream` waits for the last
@@ -182,12 +183,11 @@ ttt_status ttt_mlp_forward_static(ttt_mlp* h, const void* x, int64_t n_tokens, v
  * handle made by ttt_mlp_create_split (whose scratch may be shared) starts
  * them after everything already enqueued on `stream`.  Either way x_host is
  * read asynchronously and the results are as if everything ran on `stream`.
- * Pinned
- * (page-locked) host buffers make the copies asynchronous and let them
- * overlap; the call returns once everything is enqueued, so the caller must
- * synchronise `stream` before reading o_host or reusing x_host.  If the call
- * fails after its first segment was enqueued, copies of earlier segments may
- * still be in flight on the copy streams: synchronise the device before
+ * Pinned (page-locked) host buffers make the copies asynchronous and let
+ * them overlap; the call returns once everything is enqueued, so the caller
+ * must synchronise `stream` before reading o_host or reusing x_host.  If the
+ * call fails after its first segment was enqueued, copies of earlier segments
+ * may still be in flight on the copy streams: synchronise the device before
  * freeing or reusing the host buffers. */
 ttt_status ttt_mlp_forward_chunks_host(ttt_mlp* h, int32_t doc, const void* x_host,
                                        const void* x0_host, int64_t n_tokens,
